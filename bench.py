@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Throughput of global L2-norm gradient clipping on one GB300.
+
+One step = one clip (norm, decision and scaling) of a whole ANDREA-120M-shaped
+fp32 gradient set (124 tensors, 92,248,320 elements, one matrix spiked x50 so
+that the clip fires), through the library's C ABI, inputs resident in HBM.
+
+The metric is algorithmic bytes moved per second: 4 B per element read for the
+norm, 4 B read + 4 B written for the scaling pass, 12 B/elem = 1.107 GB per
+step.  Printed as one JSON line.
+
+Timing: a pool of P distinct copies of the gradient set; each timed run clips
+P of them back to back between two CUDA events on the launching stream.  The
+sets are larger than L2 (369 MB vs 126 MB) and L2 is flushed before each run.
+Between runs, outside the events, every set is restored from a pristine copy
+(a clip changes its input in place, and a clipped set no longer clips).
+
+--impl reference times the oracle (the plain C fp64 implementation used by the
+tests) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "global-norm clip GB/s and % of HBM roofline, ANDREA-120M fp32 grads"
+NOMINAL_HBM_GBS = 7900.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3200)
+    p.add_argument("--warmup", type=int, default=64)
+    p.add_argument("--impl", choices=["gclip", "reference"], default="gclip")
+    p.add_argument("--variant", choices=["three_kernel", "persistent"], default="persistent")
+    p.add_argument("--workload", default="andrea120m")
+    p.add_argument("--pool", type=int, default=32, help="distinct gradient sets per timed run")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="budget of the CPU-baseline leg on rank 0")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# helpers shared by both arms (host logic; covered by the CPU tests)
+
+def algorithmic_bytes(numel: int, elem_bytes: int, decision: str) -> int:
+    """Bytes a clip must move: one read for the norm; a read and a write more
+    when elements are rewritten (clip, or an unscale that is not 1)."""
+    if decision == "write":
+        return 3 * numel * elem_bytes
+    return numel * elem_bytes
+
+
+def rank_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(elapsed_ms: float, units: float, world: int, reduce_max=None):
+    """Whole-job throughput: units processed by all ranks over the slowest
+    rank's time.  reduce_max maps a local float to its max over ranks."""
+    t = reduce_max(elapsed_ms) if reduce_max else elapsed_ms
+    return units * world / (t / 1e3), t
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("gclip.cu", "plan.cpp", "internal.hpp"):
+        with open(os.path.join(ROOT, "global_l2_norm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if that summary
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "200"], stdout=self.file,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        return summarize_clocks(self.file.read())
+
+
+def summarize_clocks(text: str) -> dict:
+    sm, smax, reasons, n = [], [], set(), 0
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        n += 1
+        for name, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+
+def oracle_inputs(gs):
+    import numpy as np
+    from oracle import OracleTensor
+    out = []
+    for t in gs.tensors:
+        c = t.detach().contiguous().cpu().reshape(-1)
+        if gs.workload.dtype == "f32":
+            out.append(OracleTensor(c.numpy().copy(), "f32"))
+        elif gs.workload.dtype == "f16":
+            out.append(OracleTensor(c.numpy().copy(), "f16"))
+        else:
+            import torch
+            out.append(OracleTensor(c.view(torch.int16).numpy().view(np.uint16).copy(), "bf16"))
+    return out
+
+
+def reference_sample(gs, target_elems: int):
+    """A run of whole tensors starting at the (first) spiked matrix, about
+    target_elems elements long, so that the sample's own clip fires too."""
+    names = [s.name for s in gs.workload.layout]
+    start = names.index(gs.spiked[0]) if gs.spiked else 0
+    idx, n = [], 0
+    i = start
+    while n < target_elems and len(idx) < len(names):
+        idx.append(i)
+        n += gs.tensors[i].numel()
+        i = (i + 1) % len(names)
+    return idx, n
+
+
+def time_oracle(host, w, reps_budget_s: float):
+    import oracle
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _, r = oracle.clip(host, w.max_norm, w.inv_scale)
+        reps += 1
+        if time.perf_counter() - t0 >= reps_budget_s:
+            break
+    return (time.perf_counter() - t0) / reps, reps, r
+
+
+def run_reference(args):
+    rank, world, _ = rank_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import torch
+    from workloads import WORKLOADS, make_gradset
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    gs = make_gradset(w, device="cpu")
+    # size each step so that warmup + steps take about a minute on one core
+    calib_idx, calib_n = reference_sample(gs, 1 << 20)
+    sub = oracle_inputs(type(gs)(w, [gs.tensors[i] for i in calib_idx]))
+    t0 = time.perf_counter()
+    oracle.clip(sub, w.max_norm, w.inv_scale)
+    rate = calib_n / max(time.perf_counter() - t0, 1e-6)
+    per_step = max(1 << 16, int(rate * 60.0 / max(1, args.steps + args.warmup)))
+    per_step = min(per_step, w.numel)
+    idx, n = reference_sample(gs, per_step)
+    sub_gs = type(gs)(w, [gs.tensors[i] for i in idx], gs.spiked)
+    host = oracle_inputs(sub_gs)
+    for _ in range(args.warmup):
+        oracle.clip(host, w.max_norm, w.inv_scale)
+    times = []
+    decision = None
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, r = oracle.clip(host, w.max_norm, w.inv_scale)
+        times.append(time.perf_counter() - t0)
+        decision = r.decision_name
+    writes = decision != "skip"
+    nbytes = algorithmic_bytes(n, w.elem_bytes, "write" if writes else "read")
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    sample = (f"{len(idx)} whole tensors of the {w.name} set starting at the spiked "
+              f"matrix, {n} elements per step (decision {decision})")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / len(times) * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description,
+                   "elements_per_step": n, "bytes_per_step": nbytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the library arm
+
+def run_gclip(args):
+    import torch
+    import torch.distributed as dist
+
+    import global_l2_norm_gb300 as g
+    from workloads import WORKLOADS, make_gradset
+
+    rank, world, local = rank_env()
+    if world != args.gpus:
+        print(json.dumps({"error": f"--gpus {args.gpus} but WORLD_SIZE={world}"}))
+        return 2
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    g.build()
+    w = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(dev)
+
+    # one pristine set, P working sets
+    pristine = make_gradset(w, device=dev, flat=True)
+    P = max(1, min(args.pool, args.steps))
+    sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
+    clippers = [g.GradClipper(s.tensors, variant=args.variant) for s in sets]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 + (1 << 20), dtype=torch.uint8, device=dev)
+
+    def restore():
+        for s in sets:
+            s.flat.copy_(pristine.flat)
+        flush.fill_(1)
+
+    # correctness of the step being timed: the clip fires and the norm agrees
+    # with a float64 torch norm of the same data (a sanity check, not parity)
+    restore()
+    clippers[0].clip_(w.max_norm, w.inv_scale)
+    rec = clippers[0].result()
+    ref_norm = math.sqrt(sum(float(t.double().square().sum()) for t in pristine.tensors)
+                         ) * w.inv_scale
+    assert abs(rec["norm"] - ref_norm) <= 1e-5 * ref_norm, (rec["norm"], ref_norm)
+    writes = rec["decision"] != g.GCLIP_DECISION_SKIP and not (
+        rec["coef_hi"] == 1.0 and rec["coef_lo"] == 0.0)
+    decision_name = {0: "pass", 1: "clip", 2: "skip"}[rec["decision"]]
+    nbytes = algorithmic_bytes(w.numel, w.elem_bytes, "write" if writes else "read")
+
+    # warm-up
+    restore()
+    for i in range(args.warmup):
+        if i and i % P == 0:
+            restore()
+        clippers[i % P].clip_(w.max_norm, w.inv_scale)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    runs = []
+    done = 0
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    while done < args.steps:
+        n = min(P, args.steps - done)
+        restore()
+        e0.record(stream)
+        for i in range(n):
+            clippers[i].clip_(w.max_norm, w.inv_scale)
+        e1.record(stream)
+        e1.synchronize()
+        runs.append((e0.elapsed_time(e1), n))
+        done += n
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    local_ms = sum(t for t, _ in runs)
+
+    def reduce_max(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    value_bps, total_ms = aggregate(local_ms, nbytes * args.steps, world, reduce_max)
+    per_step_ms = total_ms / args.steps
+    step_us = sorted(t / n * 1e3 for t, n in runs)
+
+    # per-kernel durations for the roofline (events between the launches)
+    launches_per_step = 3 if args.variant == "three_kernel" else 1
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    import ctypes
+    ev_handles = (ctypes.c_void_p * 4)(*[e.cuda_event for e in evs])
+    L = g.load()
+    restore()
+    seg = [[], [], []]
+    for i in range(min(P, 16)):
+        g.check("clip_grad_norm_profiled", L.clip_grad_norm_profiled(
+            clippers[i]._h, w.max_norm, w.inv_scale, clippers[i].norm.data_ptr(),
+            clippers[i].flag.data_ptr(), stream.cuda_stream, ev_handles))
+        evs[3].synchronize()
+        for k in range(3):
+            seg[k].append(evs[k].elapsed_time(evs[k + 1]))
+    seg_ms = [statistics.mean(s) for s in seg]
+    if args.variant == "persistent":
+        kernel, k_bytes, k_ms = "k_clip_persistent", nbytes, seg_ms[2]
+        # the timed region is back-to-back launches of this one kernel
+        k_ms = per_step_ms
+    else:
+        shares = {"k_grad_norm_partial": (seg_ms[0], w.numel * w.elem_bytes),
+                  "k_grad_norm_final": (seg_ms[1], 0),
+                  "k_grad_scale": (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
+        kernel = max(shares, key=lambda k: shares[k][0])
+        k_ms, k_bytes = shares[kernel]
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs") or 6800.0
+    peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
+    achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else 0.0
+    traffic = traffic_from_profile(kernel)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
+                "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_src == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": k_bytes,
+                "launch_ms": round(k_ms, 5)}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = pristine.flat.cpu().pin_memory()
+        norm_h = torch.empty(1, dtype=torch.float32).pin_memory()
+        flag_h = torch.empty(1, dtype=torch.int32).pin_memory()
+        n_e2e = min(20, args.steps)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        times = []
+        for i in range(n_e2e + 3):
+            c = clippers[i % P]
+            flush.fill_(1)
+            s0.record(stream)
+            sets[i % P].flat.copy_(host, non_blocking=True)
+            nt, ft = c.clip_(w.max_norm, w.inv_scale)
+            norm_h.copy_(nt, non_blocking=True)
+            flag_h.copy_(ft, non_blocking=True)
+            s1.record(stream)
+            s1.synchronize()
+            assert abs(float(norm_h.item()) - rec["norm"]) <= 1e-6 * rec["norm"]
+            if i >= 3:
+                times.append(s0.elapsed_time(s1))
+        e2e_ms = reduce_max(statistics.mean(times))
+        e2e = {"value": round(nbytes * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": host.numel() * host.element_size(),
+               "d2h_bytes_per_step": norm_h.element_size() + flag_h.element_size(),
+               "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        hostset = oracle_inputs(pristine)
+        sec, reps, r = time_oracle(hostset, w, args.cpu_seconds)
+        assert r.decision_name == decision_name, (r.decision_name, decision_name)
+        cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"the whole {w.name} set ({w.numel} elements), {reps} pass(es), "
+                         f"{sec:.2f} s per pass, single-threaded C fp64 oracle"}
+
+    for c in clippers:
+        c.close()
+
+    if rank == 0:
+        value = value_bps / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {
+                "workload": w.name, "description": w.description, "tensors": len(w.layout),
+                "elements": w.numel, "bytes_per_step": nbytes, "decision": decision_name,
+                "variant": args.variant, "pool": P, "parallelism": f"replicas x{world}",
+                "l2": "inputs larger than L2 (one set per step, pool of distinct sets); "
+                      "L2 flushed before each timed run",
+                "timing": "CUDA events around each run of back-to-back clips on the "
+                          "launching stream; restores between runs outside the events",
+            },
+            "frac_of_nominal_8tbs": round(value / NOMINAL_HBM_GBS, 4),
+            "elements_per_s": round(w.numel * args.steps * world / (total_ms / 1e3), 1),
+            "us_per_step_p10_p50_p90": [round(step_us[int(q * (len(step_us) - 1))], 2)
+                                         for q in (0.1, 0.5, 0.9)],
+            "kernel_ms": {"partial": round(seg_ms[0], 5), "final": round(seg_ms[1], 5),
+                          "scale": round(seg_ms[2], 5)} if args.variant == "three_kernel"
+            else {"persistent": round(seg_ms[2], 5)},
+            "roofline": roofline,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": args.steps * launches_per_step,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gclip(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

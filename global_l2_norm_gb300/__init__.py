@@ -1,0 +1,163 @@
+"""Global L2-norm gradient clipping on one GB300 GPU.
+
+A thin Python face of the C ABI in ``include/gclip.h`` (library
+``libgclip.so``, built by :func:`build`).  PyTorch supplies device memory and
+streams; every step of the clip runs in the library's CUDA kernels.
+
+    clipper = GradClipper([p.grad for p in model.parameters()])
+    norm, flag = clipper.clip_(max_norm=1.0, inv_scale=1.0 / (loss_scale * n_micro))
+
+The clip follows "Grow a language model: gradient clipping" (unhomeschool.com),
+section "Mathematics", and "Gradient Clipping" (paweldubiel.com glossary),
+section "Mechanism and details": norm = sqrt(sum of squares over every
+element), elements scaled by max_norm / norm when norm > max_norm.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (GCLIP_BF16, GCLIP_DECISION_CLIP, GCLIP_DECISION_PASS,
+                   GCLIP_DECISION_SKIP, GCLIP_F16, GCLIP_F32, GCLIP_STATUS_OK,
+                   GCLIP_STATUS_TIMEOUT, GCLIP_VARIANT_PERSISTENT,
+                   GCLIP_VARIANT_THREE_KERNEL, GclipError, clip_chunk_t,
+                   clip_result_t, clip_tensor_desc_t, check, load)
+from ._build import build as _build_lib
+
+__all__ = ["build", "load", "GradClipper", "GclipError", "plan", "descs_for",
+           "GCLIP_F32", "GCLIP_F16", "GCLIP_BF16", "GCLIP_VARIANT_THREE_KERNEL",
+           "GCLIP_VARIANT_PERSISTENT", "GCLIP_DECISION_PASS", "GCLIP_DECISION_CLIP",
+           "GCLIP_DECISION_SKIP", "GCLIP_STATUS_OK", "GCLIP_STATUS_TIMEOUT"]
+
+DTYPE_CODES = {torch.float32: GCLIP_F32, torch.float16: GCLIP_F16,
+               torch.bfloat16: GCLIP_BF16}
+VARIANTS = {"three_kernel": GCLIP_VARIANT_THREE_KERNEL,
+            "persistent": GCLIP_VARIANT_PERSISTENT}
+
+
+def build(force: bool = False) -> str:
+    """Compile libgclip.so for sm_103a (in-tree) and load it."""
+    path = _build_lib(force=force)
+    load()
+    return path
+
+
+def descs_for(tensors) -> ctypes.Array:
+    """C descriptors for a list of contiguous tensors (any device; the
+    library only accepts CUDA memory at clip_create)."""
+    arr = (clip_tensor_desc_t * max(1, len(tensors)))()
+    for i, t in enumerate(tensors):
+        if t.dtype not in DTYPE_CODES:
+            raise TypeError(f"unsupported gradient dtype {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError("gradient tensors must be contiguous")
+        arr[i].ptr = t.data_ptr() if t.numel() else None
+        arr[i].numel = t.numel()
+        arr[i].dtype = DTYPE_CODES[t.dtype]
+        arr[i].reserved = 0
+    return arr
+
+
+def plan(descs, n: int):
+    """Host-only chunk table for `n` descriptors (no device needed)."""
+    L = load()
+    count = ctypes.c_int64()
+    check("clip_plan", L.clip_plan(descs, n, None, 0, ctypes.byref(count)))
+    table = (clip_chunk_t * max(1, count.value))()
+    check("clip_plan", L.clip_plan(descs, n, table, count.value, ctypes.byref(count)))
+    return [(table[i].addr, table[i].numel, table[i].meta) for i in range(count.value)]
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+class GradClipper:
+    """One planned clip of a fixed set of CUDA gradient tensors.
+
+    The tensors must stay allocated (same storage) for the clipper's life;
+    they are clipped in place.  Calls on one clipper must not overlap on the
+    device.
+    """
+
+    def __init__(self, tensors, variant: str | int | None = None):
+        self.tensors = list(tensors)
+        devs = {t.device for t in self.tensors}
+        if any(d.type != "cuda" for d in devs) or len(devs) > 1:
+            raise ValueError("all gradient tensors must be on one CUDA device")
+        self.device = next(iter(devs)) if devs else torch.device("cuda", torch.cuda.current_device())
+        self._lib = load()
+        descs = descs_for(self.tensors)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            check("clip_create", self._lib.clip_create(descs, len(self.tensors), ctypes.byref(h)))
+        self._h = h
+        self.norm = torch.zeros(1, dtype=torch.float32, device=self.device)
+        self.flag = torch.zeros(1, dtype=torch.int32, device=self.device)
+        if variant is not None:
+            self.set_variant(variant)
+
+    # -- the hot path -----------------------------------------------------
+    def clip_(self, max_norm: float, inv_scale: float = 1.0, stream=None,
+              out_norm: torch.Tensor | None = None, out_flag: torch.Tensor | None = None):
+        """Clip in place on `stream` (default: the current stream); returns the
+        device tensors receiving the norm (float32[1]) and the nonfinite flag
+        (int32[1]).  Nothing is synchronised."""
+        out_norm = self.norm if out_norm is None else out_norm
+        out_flag = self.flag if out_flag is None else out_flag
+        check("clip_grad_norm", self._lib.clip_grad_norm(
+            self._h, float(max_norm), float(inv_scale), out_norm.data_ptr(),
+            out_flag.data_ptr(), _stream_handle(stream, self.device)))
+        return out_norm, out_flag
+
+    # -- configuration and inspection -----------------------------------
+    def set_variant(self, variant) -> None:
+        v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+        check("clip_set_variant", self._lib.clip_set_variant(self._h, v))
+
+    @property
+    def variant(self) -> int:
+        return int(self._lib.clip_get_variant(self._h))
+
+    @property
+    def num_chunks(self) -> int:
+        return int(self._lib.clip_num_chunks(self._h))
+
+    @property
+    def persistent_grid(self) -> int:
+        return int(self._lib.clip_persistent_grid(self._h))
+
+    def result(self, stream=None) -> dict:
+        """The device record of the last call (synchronises `stream`)."""
+        r = clip_result_t()
+        check("clip_read_result", self._lib.clip_read_result(
+            self._h, ctypes.byref(r), _stream_handle(stream, self.device)))
+        return {k: getattr(r, k) for k, _ in clip_result_t._fields_ if k != "reserved"}
+
+    def reset(self, stream=None) -> None:
+        check("clip_reset", self._lib.clip_reset(self._h, _stream_handle(stream, self.device)))
+
+    def debug_barrier(self, extra_arrivals: int, timeout_ns: int = 0) -> None:
+        check("clip_debug_barrier", self._lib.clip_debug_barrier(
+            self._h, int(extra_arrivals), int(timeout_ns)))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            check("clip_destroy", self._lib.clip_destroy(self._h))
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

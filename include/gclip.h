@@ -1,0 +1,251 @@
+/*
+ * gclip.h -- global L2-norm gradient clipping on one GB300 GPU (sm_103a).
+ *
+ * The operation.  "Grow a language model: gradient clipping"
+ * (unhomeschool.com, Russian), section "Mathematics": treat every gradient
+ * element of every parameter as one vector g; norm = sqrt(sum g_i^2); if
+ * norm <= max_norm the gradients pass unchanged, otherwise each element is
+ * multiplied by max_norm / norm.  "Gradient Clipping" (paweldubiel.com
+ * glossary), section "Mechanism and details": the same piecewise rule for a
+ * threshold c > 0, with the comparison strict.  The clip runs once per
+ * optimizer step, after gradient accumulation, averaging and loss-scale
+ * unscaling (glossary, "Order changes the result"; "Grow a language model:
+ * backprop", section "Accumulation across microbatches") and before the AdamW
+ * moments and weights are updated (clipping page, "Order matters: Pre-Adam").
+ *
+ * The library works in place on the caller's gradient buffers, on the device,
+ * asynchronously on the caller's stream.  It never synchronises the host with
+ * the device inside clip_grad_norm and never allocates there: every buffer is
+ * allocated once in clip_create (the backprop page, section "Cost of general
+ * frameworks": buffers are preallocated at start-up, never reallocated).
+ *
+ * Return codes are synchronous, host-side checks of the arguments and of the
+ * CUDA launch.  Results that depend on the data (the norm, the nonfinite
+ * flag, the decision, a timeout of the single-launch variant's grid barrier)
+ * are written to device memory and never returned by these calls.
+ */
+#ifndef GCLIP_H
+#define GCLIP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define GCLIP_OK 0
+#define GCLIP_ERR_INVALID_ARG 1  /* a host-side argument check failed      */
+#define GCLIP_ERR_OOM 2          /* device or host allocation failed       */
+#define GCLIP_ERR_CUDA 3         /* a CUDA runtime call or launch failed   */
+#define GCLIP_ERR_UNSUPPORTED 4  /* the device cannot run the request      */
+
+/* ---- values written to clip_result_t.status on the device -------------- */
+#define GCLIP_STATUS_OK 0
+#define GCLIP_STATUS_TIMEOUT 1   /* single-launch variant: a CTA gave up
+                                    waiting at the grid barrier; see
+                                    clip_reset */
+
+/* ---- element formats of a gradient tensor ------------------------------ */
+#define GCLIP_F32 0              /* IEEE binary32                          */
+#define GCLIP_F16 1              /* IEEE binary16                          */
+#define GCLIP_BF16 2             /* bfloat16 (upper half of a binary32)    */
+
+/* ---- clip decisions (clip_result_t.decision) --------------------------- */
+#define GCLIP_DECISION_PASS 0    /* norm <= max_norm: only the unscale (if
+                                    inv_scale != 1) was written            */
+#define GCLIP_DECISION_CLIP 1    /* norm > max_norm: every element scaled  */
+#define GCLIP_DECISION_SKIP 2    /* nonfinite: no element was written      */
+
+/* ---- execution variants (clip_set_variant) ----------------------------- */
+#define GCLIP_VARIANT_THREE_KERNEL 0  /* partial sums, final reduce, scale:
+                                         three launches (the clipping page,
+                                         "ANDREA's three-kernel pipeline")  */
+#define GCLIP_VARIANT_PERSISTENT 1    /* the same three steps in one
+                                         cooperative launch with a
+                                         last-CTA-done reduction            */
+
+/* One gradient tensor: `numel` elements of format `dtype`, contiguous, in
+ * device memory at `ptr` (aligned to the element size).  `reserved` must be
+ * 0.  Tensors of one handle must not overlap. */
+typedef struct {
+    void *ptr;
+    int64_t numel;
+    int32_t dtype;
+    int32_t reserved;
+} clip_tensor_desc_t;
+
+/* The device-resident record of the last call on a handle.  The multiplier
+ * that was applied to every element x is coef_hi + coef_lo (a float-float
+ * pair; the product x * inv_scale * max_norm / norm for CLIP, x * inv_scale
+ * for PASS).  sumsq_hi + sumsq_lo is the sum of squares of the unscaled
+ * gradients. */
+typedef struct {
+    float norm;          /* global norm of the unscaled gradients (fp32)   */
+    int32_t nonfinite;   /* 1 if an element is NaN/inf or the sum of
+                            squares exceeds the largest finite fp32 value  */
+    int32_t decision;    /* GCLIP_DECISION_*                               */
+    int32_t status;      /* GCLIP_STATUS_*                                 */
+    float coef_hi;
+    float coef_lo;
+    float sumsq_hi;
+    float sumsq_lo;
+    uint32_t calls;      /* completed calls on this handle (wraps)         */
+    int32_t reserved;
+} clip_result_t;
+
+/* One entry of the chunk table: a run of one tensor, handled by one thread
+ * block: at most GCLIP_CHUNK_BYTES, plus, for the first chunk of a tensor,
+ * the fewer than 16 bytes that precede the tensor's first 16-byte boundary. */
+typedef struct {
+    uint64_t addr;       /* device address of the first element            */
+    uint32_t numel;      /* elements in this chunk                         */
+    uint32_t meta;       /* bits 0-7: dtype; bits 8-31: tensor index       */
+} clip_chunk_t;
+
+#define GCLIP_CHUNK_BYTES 32768
+#define GCLIP_MAX_TENSORS (1 << 24)
+
+typedef struct gclip_handle *clip_handle_t;
+
+/* clip_create -- plan the clip of one fixed set of gradient tensors.
+ *
+ * Source: the clipping page, section "ANDREA's three-kernel pipeline": the
+ * work is cut into fragments, one thread block per fragment, hundreds of
+ * blocks across all tensors of very different shapes (section "Why computing
+ * the grad norm needs three kernels": embedding 8449x768 next to layer norm
+ * [768]).  This call builds that fragment (chunk) table once, on the host,
+ * uploads it, and allocates the per-chunk scratch of partial sums and the
+ * result record on the current CUDA device.  It is the only call that
+ * allocates.
+ *
+ * descs, n_tensors: host array of the gradient tensors, in the order their
+ *   squares are summed; copied, so the array may be freed on return.  The
+ *   tensors themselves stay owned by the caller, who must keep them
+ *   allocated, at the same addresses, until clip_destroy.
+ * out: receives the new handle (owned by the caller; free with clip_destroy).
+ * Returns GCLIP_OK; GCLIP_ERR_INVALID_ARG if out is NULL, n_tensors < 0 or
+ *   > GCLIP_MAX_TENSORS, descs is NULL with n_tensors > 0, a numel is < 0, a
+ *   dtype is unknown, reserved != 0, ptr is NULL or misaligned for a
+ *   non-empty tensor, or two non-empty tensors overlap; GCLIP_ERR_OOM or
+ *   GCLIP_ERR_CUDA from the device.  *out is untouched on error. */
+int clip_create(const clip_tensor_desc_t *descs, int32_t n_tensors,
+                clip_handle_t *out);
+
+/* clip_grad_norm -- clip the handle's gradients in place by their global
+ * L2 norm.
+ *
+ * Source: the clipping page, section "Mathematics" (norm, strict test,
+ * factor max_norm / norm) and section "ANDREA's three-kernel pipeline"
+ * (partial sums of squares per fragment into a scratch buffer, one reduction
+ * to a scalar and its square root, one scaling pass); the glossary page,
+ * "Mechanism and details" (c > 0) and "Order changes the result" (unscale
+ * before the threshold); the backprop page, "Accumulation across
+ * microbatches" (average by 1/n_microbatches).
+ *
+ * Each element x is read in its own format and widened to fp32; the norm is
+ * that of y = x * inv_scale, so inv_scale = 1 / (loss_scale * n_microbatches)
+ * folds the unscale and the average into the clip.  If any element is NaN or
+ * infinite (or the sum of squares overflows fp32) the decision is SKIP and no
+ * element is written (the glossary, "Shorten the arrow": a nonfinite value
+ * stops the update).  Otherwise, if norm > max_norm, every element becomes
+ * x * inv_scale * max_norm / norm (CLIP); else x * inv_scale (PASS), and when
+ * that multiplier is exactly 1 nothing is written at all.  Results are rounded
+ * to nearest-even into the tensor's own format.
+ *
+ * The sum is taken in a fixed order (per chunk, then over chunks) with a
+ * float-float accumulator, so the norm is bit-identical from run to run and
+ * between the two variants.
+ *
+ * max_norm: threshold c, finite and > 0.  inv_scale: finite and > 0.
+ * out_norm: device float, may be NULL; receives the norm (fp32).
+ * out_nonfinite_flag: device int32, may be NULL; receives 0 or 1.
+ * stream: a cudaStream_t of the handle's device (NULL = legacy default).
+ * Asynchronous: returns after enqueueing.  Calls on one handle must not
+ * overlap on the device (they share the scratch).
+ * Returns GCLIP_OK; GCLIP_ERR_INVALID_ARG for a NULL handle or a bad
+ *   max_norm / inv_scale (nothing is enqueued then); GCLIP_ERR_CUDA if a
+ *   launch failed. */
+int clip_grad_norm(clip_handle_t h, float max_norm, float inv_scale,
+                   float *out_norm, int32_t *out_nonfinite_flag, void *stream);
+
+/* clip_grad_norm_profiled -- clip_grad_norm that also records four CUDA
+ * events (cudaEvent_t handles created by the caller on the handle's device)
+ * on `stream`: events[0] before the first launch, events[1] after the
+ * partial sums, events[2] after the final reduction, events[3] after the
+ * scaling pass.  With the single-launch variant the one launch lies between
+ * events[0] and events[3], and events[1] and events[2] are recorded with
+ * events[0].  Programmatic dependent launch is not used in this mode, so the
+ * kernels do not overlap their neighbours; it is meant for measuring each
+ * step of the clip, with the same arithmetic and results as clip_grad_norm.
+ * Returns as clip_grad_norm, and GCLIP_ERR_INVALID_ARG for NULL events. */
+int clip_grad_norm_profiled(clip_handle_t h, float max_norm, float inv_scale,
+                            float *out_norm, int32_t *out_nonfinite_flag,
+                            void *stream, void *const *events);
+
+/* clip_destroy -- wait for the handle's device work, free its device memory
+ * and the handle.  NULL is accepted and ignored.  Returns GCLIP_OK, or
+ * GCLIP_ERR_CUDA if the device reported an error while finishing. */
+int clip_destroy(clip_handle_t h);
+
+/* clip_set_variant -- choose GCLIP_VARIANT_THREE_KERNEL or
+ * GCLIP_VARIANT_PERSISTENT for later calls.  Both compute bit-identical
+ * norms and outputs.  Returns GCLIP_ERR_INVALID_ARG for an unknown variant,
+ * GCLIP_ERR_UNSUPPORTED if the device cannot launch cooperative kernels. */
+int clip_set_variant(clip_handle_t h, int32_t variant);
+
+/* clip_get_variant -- the variant in use, or -1 for a NULL handle. */
+int32_t clip_get_variant(clip_handle_t h);
+
+/* clip_result_device -- device address of the handle's clip_result_t,
+ * valid until clip_destroy; NULL for a NULL handle.  Stream-ordered reads of
+ * it after a call see that call's record. */
+const clip_result_t *clip_result_device(clip_handle_t h);
+
+/* clip_read_result -- copy the record to host memory `out`, synchronising
+ * `stream` (inspection and tests; not for the training loop).  Returns
+ * GCLIP_ERR_INVALID_ARG for NULL arguments, GCLIP_ERR_CUDA on failure. */
+int clip_read_result(clip_handle_t h, clip_result_t *out, void *stream);
+
+/* clip_reset -- enqueue a clear of the handle's grid-barrier words and of
+ * the status in its record.  Needed only after a call reported
+ * GCLIP_STATUS_TIMEOUT, whose gradients are then in an unspecified state
+ * (some chunks may have been scaled).  Returns GCLIP_OK or GCLIP_ERR_*. */
+int clip_reset(clip_handle_t h, void *stream);
+
+/* clip_num_chunks -- chunks in the handle's table (-1 for NULL). */
+int64_t clip_num_chunks(clip_handle_t h);
+
+/* clip_persistent_grid -- thread blocks of the single-launch variant on this
+ * handle's device (-1 for NULL). */
+int32_t clip_persistent_grid(clip_handle_t h);
+
+/* clip_plan -- host-only: validate `descs` exactly as clip_create does and
+ * write the chunk table it would build into `out` (capacity entries, may be
+ * NULL to count).  Chunks follow tensor order; within a tensor they are
+ * consecutive and sized as clip_chunk_t states, and every chunk after a
+ * tensor's first starts on a 16-byte boundary.  Empty tensors get no chunk.
+ * *n_chunks receives the count.  Touches no device.  Returns GCLIP_OK,
+ * GCLIP_ERR_INVALID_ARG (as clip_create, or capacity too small for a
+ * non-NULL out). */
+int clip_plan(const clip_tensor_desc_t *descs, int32_t n_tensors,
+              clip_chunk_t *out, int64_t capacity, int64_t *n_chunks);
+
+/* clip_status_string -- a static English description of a return code. */
+const char *clip_status_string(int32_t code);
+
+/* clip_debug_barrier -- test hook for the single-launch variant's bounded
+ * grid barrier.  extra_arrivals > 0 makes the barrier wait for that many
+ * more thread blocks than exist, so it cannot complete and every block must
+ * give up after timeout_ns (0 keeps the default of one second), write
+ * GCLIP_STATUS_TIMEOUT and return without writing gradients.  The library
+ * clears the barrier words around such a call.  extra_arrivals = 0 restores
+ * normal operation.  Returns GCLIP_OK or GCLIP_ERR_INVALID_ARG. */
+int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals,
+                       int64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCLIP_H */

@@ -106,6 +106,11 @@ class Oracle:
         L.oracle_clip.restype = ctypes.c_int
         L.oracle_clip_per_tensor.argtypes = L.oracle_clip.argtypes
         L.oracle_clip_per_tensor.restype = ctypes.c_int
+        L.oracle_clip_sample.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int32,
+                                         ctypes.c_double, ctypes.c_double, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.POINTER(_Result)]
+        L.oracle_clip_sample.restype = ctypes.c_int
         L.oracle_sumsq.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int32,
                                    ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_int32)]
@@ -143,6 +148,22 @@ class Oracle:
             raise ValueError("oracle_clip rejected its arguments")
         return outs, OracleResult(res.sumsq, res.norm, res.coef,
                                   bool(res.nonfinite), res.decision)
+
+    def clip_sample(self, tensors, max_norm: float, inv_scale, tensor_idx, elem_idx):
+        """The clip of the whole set, with the outputs of only the chosen
+        elements: returns (list of storage arrays, one value per sample in its
+        tensor's format, OracleResult)."""
+        ti = np.ascontiguousarray(tensor_idx, dtype=np.int32)
+        ei = np.ascontiguousarray(elem_idx, dtype=np.int64)
+        slots = np.zeros(ti.size, dtype=np.uint32)
+        res = _Result()
+        rc = self._lib.oracle_clip_sample(self._descs(tensors), len(tensors), float(max_norm),
+                                          float(inv_scale), ti.ctypes.data, ei.ctypes.data,
+                                          ti.size, slots.ctypes.data, ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_clip_sample rejected its arguments")
+        return slots, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
+                                   res.decision)
 
     def clip_per_tensor(self, tensors, max_norm: float, inv_scale: float = 1.0):
         outs = [OracleTensor(t.data.copy(), t.dtype) for t in tensors]

@@ -274,23 +274,15 @@ int oracle_sumsq(const oracle_tensor *ts, int32_t n_tensors, double inv_scale,
     return 0;
 }
 
-/* Global-norm clip.  `in` and `out` describe the same shapes and dtypes;
- * out[t].data is writable host memory (it may equal in[t].data).  On SKIP
- * the input bits are copied unchanged; on PASS and CLIP every element is
- * rewritten as round(x * inv_scale * coef) in its own format.
- * Returns 0, or -1 for bad arguments (c <= 0 or nonfinite, inv_scale <= 0 or
- * nonfinite, malformed or mismatched descriptors). */
-int oracle_clip(const oracle_tensor *in, const oracle_tensor *out,
-                int32_t n_tensors, double max_norm, double inv_scale,
-                oracle_result *res)
+/* The decision: sum of squares, norm, nonfinite flag, clip or pass, and the
+ * multiplier.  Returns 0, or -1 for bad arguments (c <= 0 or nonfinite,
+ * inv_scale <= 0 or nonfinite, malformed descriptors). */
+static int decide(const oracle_tensor *in, int32_t n_tensors, double max_norm,
+                  double inv_scale, oracle_result *res)
 {
     if (!(max_norm > 0.0) || !isfinite(max_norm) || !(inv_scale > 0.0) ||
         !isfinite(inv_scale) || n_tensors < 0)
         return -1;
-    for (int32_t t = 0; t < n_tensors; ++t)
-        if (out[t].numel != in[t].numel || out[t].dtype != in[t].dtype)
-            return -1;
-
     double s;
     int32_t nf;
     if (oracle_sumsq(in, n_tensors, inv_scale, &s, &nf) != 0)
@@ -321,11 +313,45 @@ int oracle_clip(const oracle_tensor *in, const oracle_tensor *out,
         decision = OR_DECISION_PASS;
         coef = 1.0;
     }
+    res->sumsq = s;
+    res->norm = norm;
+    res->coef = coef;
+    res->nonfinite = nf;
+    res->decision = decision;
+    return 0;
+}
+
+/* The clipped value of one element, before rounding to its format. */
+static double clipped_value(double x, double inv_scale, double coef)
+{
+#if ORACLE_MUTANT == 9
+    return x * coef;                           /* mistake: output not unscaled */
+#elif ORACLE_MUTANT == 10
+    return -x * inv_scale * coef;              /* mistake: sign flipped */
+#else
+    return x * inv_scale * coef;
+#endif
+}
+
+/* Global-norm clip.  `in` and `out` describe the same shapes and dtypes;
+ * out[t].data is writable host memory (it may equal in[t].data).  On SKIP
+ * the input bits are copied unchanged; on PASS and CLIP every element is
+ * rewritten as round(x * inv_scale * coef) in its own format.
+ * Returns 0, or -1 for bad arguments. */
+int oracle_clip(const oracle_tensor *in, const oracle_tensor *out,
+                int32_t n_tensors, double max_norm, double inv_scale,
+                oracle_result *res)
+{
+    for (int32_t t = 0; t < n_tensors; ++t)
+        if (out[t].numel != in[t].numel || out[t].dtype != in[t].dtype)
+            return -1;
+    if (decide(in, n_tensors, max_norm, inv_scale, res) != 0)
+        return -1;
 
     for (int32_t t = 0; t < n_tensors; ++t) {
         int64_t n = in[t].numel;
         int32_t dt = in[t].dtype;
-        if (decision == OR_DECISION_SKIP) {
+        if (res->decision == OR_DECISION_SKIP) {
             if (out[t].data != in[t].data)
                 memcpy((void *)out[t].data, in[t].data,
                        (size_t)n * (size_t)elem_size(dt));
@@ -333,22 +359,39 @@ int oracle_clip(const oracle_tensor *in, const oracle_tensor *out,
         }
         for (int64_t i = 0; i < n; ++i) {
             double x = oracle_decode(in[t].data, i, dt);
-#if ORACLE_MUTANT == 9
-            double v = x * coef;               /* mistake: output not unscaled */
-#elif ORACLE_MUTANT == 10
-            double v = -x * inv_scale * coef;  /* mistake: sign flipped */
-#else
-            double v = x * inv_scale * coef;
-#endif
-            oracle_encode((void *)out[t].data, i, dt, v);
+            oracle_encode((void *)out[t].data, i, dt,
+                          clipped_value(x, inv_scale, res->coef));
         }
     }
+    return 0;
+}
 
-    res->sumsq = s;
-    res->norm = norm;
-    res->coef = coef;
-    res->nonfinite = nf;
-    res->decision = decision;
+/* The same clip with the outputs of only `k` chosen elements: element
+ * elem[j] of tensor tensor[j] is written, in its tensor's storage format, to
+ * out_storage at byte offset 4*j (fp32) or 2*j (fp16/bf16 use the low half
+ * of a 4-byte slot).  For sets too large to rewrite whole in the tests.
+ * Returns 0, or -1 for bad arguments or an index out of range. */
+int oracle_clip_sample(const oracle_tensor *in, int32_t n_tensors,
+                       double max_norm, double inv_scale,
+                       const int32_t *tensor, const int64_t *elem, int64_t k,
+                       void *out_storage, oracle_result *res)
+{
+    if (decide(in, n_tensors, max_norm, inv_scale, res) != 0)
+        return -1;
+    for (int64_t j = 0; j < k; ++j) {
+        int32_t t = tensor[j];
+        if (t < 0 || t >= n_tensors || elem[j] < 0 || elem[j] >= in[t].numel)
+            return -1;
+        int32_t dt = in[t].dtype;
+        char *slot = (char *)out_storage + 4 * j;
+        if (res->decision == OR_DECISION_SKIP) {
+            memcpy(slot, (const char *)in[t].data + elem_size(dt) * elem[j],
+                   (size_t)elem_size(dt));
+            continue;
+        }
+        double x = oracle_decode(in[t].data, elem[j], dt);
+        oracle_encode(slot, 0, dt, clipped_value(x, inv_scale, res->coef));
+    }
     return 0;
 }
 

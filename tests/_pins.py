@@ -349,4 +349,21 @@ def pin_round_grid_matches_c_cast(o):
     assert np.array_equal(got, want)
 
 
+def pin_sampled_outputs_match_full_clip(o):
+    """The sampled-output entry point returns, at every chosen element, the
+    bits the full clip writes there, and the same decision."""
+    rng = np.random.default_rng(12)
+    ts = [make(rng.normal(0, 1, n), dt) for n, dt in ((40, "f32"), (33, "f16"), (9, "bf16"))]
+    for c, s in ((2.0, 1.0), (50.0, 0.5), (0.1, 2.0 ** -4)):
+        outs, r = o.clip(ts, c, s)
+        ti = np.repeat(np.arange(3), [40, 33, 9])
+        ei = np.concatenate([np.arange(40), np.arange(33), np.arange(9)])
+        slots, rs = o.clip_sample(ts, c, s, ti, ei)
+        assert rs.decision == r.decision and rs.norm == r.norm
+        got = np.concatenate([slots[:40], slots[40:73] & 0xFFFF, slots[73:] & 0xFFFF])
+        want = np.concatenate([outs[0].data.view(np.uint32), outs[1].data.view(np.uint16),
+                               outs[2].data]).astype(np.uint32)
+        assert np.array_equal(got, want)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

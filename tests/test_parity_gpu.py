@@ -1,0 +1,296 @@
+"""Parity of the CUDA path with the oracle, through the C ABI, on the GPU."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import global_l2_norm_gb300 as g
+import oracle
+from _gpu import clone_all, compare, gpu_clip, host_copies, restore
+from _helpers import golden, storage_bits, to_oracle, ulp_distance
+from oracle import OracleTensor
+from workloads import WORKLOADS, make_gradset
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["three_kernel", "persistent"]
+TD = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    g.build()
+
+
+def dev():
+    return torch.device("cuda", 0)
+
+
+# -- the pages' worked example -----------------------------------------------
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_worked_example(variant, dt):
+    ex = golden("worked_example.txt")
+    x = torch.tensor(ex["input"], dtype=TD[dt], device=dev())
+    rec = gpu_clip([x], ex["threshold"], variant=variant)
+    assert rec["norm"] == ex["norm"] and rec["decision"] == g.GCLIP_DECISION_CLIP
+    assert x.double().cpu().tolist() == ex["output"]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_boundary_passes_without_writing(variant):
+    ex = golden("boundary_passthrough.txt")
+    for c in (ex["threshold_boundary"], ex["threshold_above"]):
+        x = torch.tensor(ex["input"], dtype=torch.float32, device=dev())
+        rec = gpu_clip([x], c, variant=variant)
+        assert rec["decision"] == g.GCLIP_DECISION_PASS
+        assert x.cpu().tolist() == ex["output"]
+        assert rec["coef_hi"] == 1.0 and rec["coef_lo"] == 0.0
+
+
+# -- seeded workloads ----------------------------------------------------------
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "andrea14m"])
+def test_small_workloads(variant, name):
+    gs = make_gradset(name, device=dev())
+    before = host_copies(gs.tensors)
+    rec = gpu_clip(gs.tensors, gs.max_norm, gs.inv_scale, variant)
+    res = compare(before, gs.tensors, rec, gs.max_norm, gs.inv_scale, name)
+    expect = {"tiny": oracle.CLIP, "andrea14m": oracle.PASS}[name]
+    assert res["oracle"].decision == expect
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["andrea120m", "andrea120m_fp16", "andrea120m_fp16_inf",
+                                  "andrea120m_bf16"])
+def test_andrea120m(variant, name):
+    gs = make_gradset(name, device=dev())
+    before = host_copies(gs.tensors)
+    rec = gpu_clip(gs.tensors, gs.max_norm, gs.inv_scale, variant)
+    res = compare(before, gs.tensors, rec, gs.max_norm, gs.inv_scale, name)
+    expect = {"andrea120m": oracle.CLIP, "andrea120m_bf16": oracle.CLIP,
+              "andrea120m_fp16": oracle.PASS, "andrea120m_fp16_inf": oracle.SKIP}[name]
+    assert res["oracle"].decision == expect
+    if name == "andrea120m_fp16":
+        # the unscale by 2^-18 is exact before the final rounding: bit-exact
+        assert res["worst_ulp"]["f16"] == 0
+
+
+def test_andrea1p2b():
+    gs = make_gradset("andrea1p2b", device=dev())
+    before = host_copies(gs.tensors)
+    rec = gpu_clip(gs.tensors, gs.max_norm, gs.inv_scale, "persistent")
+    res = compare(before, gs.tensors, rec, gs.max_norm, gs.inv_scale, "andrea1p2b")
+    assert res["oracle"].decision == oracle.CLIP
+
+
+# -- ragged, misaligned, mixed, guarded ----------------------------------------
+
+SIZES = [0, 1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 33, 255, 256, 257, 1023, 2047, 4095,
+         8191, 8192, 8193, 16383, 16384, 16385, 100003]
+GUARD = 64  # bytes of sentinel on each side of every tensor
+
+
+def carve(sizes, dtypes, offsets, seed):
+    """Tensors cut from one byte buffer at the given element offsets, with
+    sentinel bands between them."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    layout, pos = [], 0
+    for n, dt, off in zip(sizes, dtypes, offsets):
+        es = 4 if dt == "f32" else 2
+        pos += GUARD
+        pos = (pos + 15) // 16 * 16 + off * es
+        layout.append((pos, n, dt))
+        pos += n * es
+    pos += GUARD
+    buf = torch.full((pos,), 0xA5, dtype=torch.uint8, device=dev())
+    tensors = []
+    for p, n, dt in layout:
+        es = 4 if dt == "f32" else 2
+        t = buf[p:p + n * es].view(TD[dt])
+        vals = torch.randn(n, generator=gen) * 0.5
+        t.copy_(vals.to(TD[dt]).to(dev()))
+        tensors.append(t)
+    return buf, layout, tensors
+
+
+def guards_intact(buf, layout):
+    mask = torch.ones(buf.numel(), dtype=torch.bool, device=buf.device)
+    for p, n, dt in layout:
+        es = 4 if dt == "f32" else 2
+        mask[p:p + n * es] = False
+    return bool((buf[mask] == 0xA5).all())
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("max_norm,inv_scale", [(1.0, 1.0), (1e6, 1.0), (2.0, 2.0 ** -10),
+                                                (1e6, 2.0 ** -3), (0.5, 0.3)])
+def test_ragged_mixed_guarded(variant, max_norm, inv_scale):
+    rng = np.random.default_rng(17)
+    dts = [str(rng.choice(["f32", "f16", "bf16"])) for _ in SIZES]
+    offs = [int(rng.integers(0, 8)) for _ in SIZES]
+    buf, layout, ts = carve(SIZES, dts, [o % (4 if d == "f32" else 8) for o, d in zip(offs, dts)], 5)
+    before = host_copies(ts)
+    inv = float(np.float32(inv_scale))
+    rec = gpu_clip(ts, max_norm, inv, variant)
+    compare(before, ts, rec, max_norm, inv, "ragged")
+    assert guards_intact(buf, layout)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_every_size_alone(variant):
+    """Each ragged size as a one-tensor set at every misalignment."""
+    for n in [1, 3, 5, 17, 257, 8191, 8193, 16385]:
+        for dt in ("f32", "f16", "bf16"):
+            per = 4 if dt == "f32" else 8
+            for off in range(per):
+                buf, layout, ts = carve([n], [dt], [off], n * 31 + off)
+                before = host_copies(ts)
+                rec = gpu_clip(ts, 0.25, 1.0, variant)
+                compare(before, ts, rec, 0.25, 1.0, f"{dt}:{n}:{off}")
+                assert guards_intact(buf, layout)
+
+
+# -- edge cases -------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_empty_sets(variant):
+    rec = gpu_clip([], 1.0, variant=variant)
+    assert rec["norm"] == 0.0 and rec["decision"] == g.GCLIP_DECISION_PASS
+    e = torch.empty(0, device=dev())
+    rec = gpu_clip([e, e.clone()], 1.0, variant=variant)
+    assert rec["norm"] == 0.0 and rec["nonfinite"] == 0
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("bad", [math.inf, -math.inf, math.nan])
+def test_nonfinite_leaves_everything(variant, bad):
+    gs = make_gradset("andrea14m", device=dev())
+    gs.tensors[5].view(-1)[1234] = bad
+    before = host_copies(gs.tensors)
+    rec = gpu_clip(gs.tensors, 1e-3, 1.0, variant)
+    assert rec["nonfinite"] == 1 and rec["decision"] == g.GCLIP_DECISION_SKIP
+    compare(before, gs.tensors, rec, 1e-3, 1.0, "nonfinite")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_overflow_counts_as_nonfinite(variant):
+    x = torch.tensor([2e19, 1.0, 3.0], device=dev())
+    before = host_copies([x])
+    rec = gpu_clip([x], 1.0, 1.0, variant)
+    assert rec["nonfinite"] == 1
+    compare(before, [x], rec, 1.0, 1.0, "overflow")
+
+
+def test_largest_tensor_64bit_offsets():
+    """One fp16 tensor of 2^31 + 37 elements (4.3 GB): chunk addresses past
+    2^32 bytes; the norm against the oracle, outputs on a sample (both ends
+    and 4096 random elements) that the oracle computes one by one."""
+    n = 2 ** 31 + 37
+    x = torch.empty(n, dtype=torch.float16, device=dev())
+    gen = torch.Generator(device=dev()).manual_seed(99)
+    x.normal_(0.0, 1.0, generator=gen)
+    host = to_oracle(x)
+    with g.GradClipper([x]) as c:
+        c.clip_(100.0, 1.0)
+        rec = c.result()
+    idx = np.concatenate([np.arange(0, 64), np.arange(n - 64, n),
+                          np.random.default_rng(1).integers(0, n, 4096)])
+    slots, r = oracle.default().clip_sample([host], 100.0, 1.0, np.zeros(idx.size), idx)
+    assert rec["decision"] == r.decision == oracle.CLIP
+    assert abs(rec["norm"] - r.norm) / r.norm < 1e-5
+    got = x[torch.from_numpy(idx).to(dev())].cpu().numpy()
+    want = (slots & 0xFFFF).astype(np.uint16).view(np.float16)
+    d = ulp_distance(OracleTensor(got, "f16"), OracleTensor(want, "f16"))
+    assert d.max() <= 1
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_null_outputs_and_side_stream(variant):
+    gs = make_gradset("tiny", device=dev())
+    before = host_copies(gs.tensors)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with g.GradClipper(gs.tensors, variant=variant) as c:
+        L = g.load()
+        assert L.clip_grad_norm(c._h, 1.0, 1.0, None, None, s.cuda_stream) == 0
+        rec = c.result(stream=s)
+    rec["out_norm"], rec["out_flag"] = rec["norm"], rec["nonfinite"]
+    compare(before, gs.tensors, rec, 1.0, 1.0, "stream")
+
+
+def test_scalar_arguments_rejected():
+    x = torch.ones(8, device=dev())
+    with g.GradClipper([x]) as c:
+        L = g.load()
+        for m, s in ((0.0, 1.0), (-1.0, 1.0), (math.nan, 1.0), (math.inf, 1.0),
+                     (1.0, 0.0), (1.0, -1.0), (1.0, math.inf)):
+            assert L.clip_grad_norm(c._h, m, s, None, None, None) == g._abi.GCLIP_ERR_INVALID_ARG
+        assert L.clip_set_variant(c._h, 7) == g._abi.GCLIP_ERR_INVALID_ARG
+    assert x.cpu().tolist() == [1.0] * 8
+
+
+def test_rejects_host_memory_descriptor():
+    """Host tensors are not device memory; the library must not be handed
+    them (the binding refuses before the C call)."""
+    with pytest.raises(ValueError):
+        g.GradClipper([torch.ones(4)])
+
+
+# -- determinism ----------------------------------------------------------------
+
+def test_bit_identical_runs_and_variants():
+    gs = make_gradset("andrea120m", device=dev())
+    pristine = clone_all(gs.tensors)
+    records, outs = [], []
+    with g.GradClipper(gs.tensors) as c:
+        for i in range(20):
+            c.set_variant("three_kernel" if i % 2 == 0 else "persistent")
+            restore(gs.tensors, pristine)
+            c.clip_(gs.max_norm, gs.inv_scale)
+            r = c.result()
+            records.append((r["norm"], r["sumsq_hi"], r["sumsq_lo"], r["coef_hi"], r["coef_lo"]))
+            if i < 2:
+                outs.append([storage_bits(to_oracle(t)) for t in gs.tensors[:6]])
+    assert len(set(records)) == 1, set(records)
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+
+
+def test_clip_twice_is_stable():
+    """After a clip the norm is max_norm: a second call sees norm ~= 1."""
+    gs = make_gradset("andrea14m", device=dev())
+    for t in gs.tensors:
+        t.mul_(100.0)
+    with g.GradClipper(gs.tensors) as c:
+        c.clip_(1.0)
+        first = c.result()
+        c.clip_(1.0)
+        second = c.result()
+    assert first["decision"] == g.GCLIP_DECISION_CLIP
+    assert abs(second["norm"] - 1.0) < 1e-6
+
+
+# -- the single-launch variant's bounded barrier --------------------------------
+
+def test_barrier_timeout_reports_and_writes_nothing():
+    gs = make_gradset("andrea14m", device=dev())
+    before = host_copies(gs.tensors)
+    with g.GradClipper(gs.tensors, variant="persistent") as c:
+        c.debug_barrier(1, 20_000_000)     # one arrival that never comes; 20 ms
+        c.clip_(1e-3)
+        rec = c.result()
+        assert rec["status"] == g.GCLIP_STATUS_TIMEOUT
+        for b, t in zip(before, gs.tensors):
+            assert np.array_equal(storage_bits(b), storage_bits(to_oracle(t)))
+        c.debug_barrier(0)
+        c.reset()
+        c.clip_(1e-3)
+        rec = c.result()
+        assert rec["status"] == g.GCLIP_STATUS_OK
+        assert rec["decision"] == g.GCLIP_DECISION_CLIP
+    rec["out_norm"], rec["out_flag"] = rec["norm"], rec["nonfinite"]
+    compare(before, gs.tensors, rec, 1e-3, 1.0, "after-timeout")

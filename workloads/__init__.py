@@ -123,6 +123,7 @@ class GradSet:
     tensors: list
     spiked: list = field(default_factory=list)   # names of the spiked tensors
     inf_at: tuple | None = None                  # (tensor index, flat index)
+    flat: object = None                          # the single buffer, if flat
 
     @property
     def max_norm(self) -> float:
@@ -146,24 +147,43 @@ def _choices(seed: int, layout, w: Workload):
     return spiked, inf_at
 
 
-def make_gradset(name_or_workload, seed: int = SEED, device="cpu") -> GradSet:
+def make_gradset(name_or_workload, seed: int = SEED, device="cpu", flat: bool = False) -> GradSet:
     """Allocate and fill one gradient set.  Values come from torch's generator
     on `device` seeded with `seed`, so a set is reproducible on a given kind of
     device; parity tests hand the oracle a host copy of the very tensors the
-    GPU sees."""
+    GPU sees.  With flat=True every tensor is a view into one buffer (each
+    starting on a 256-byte boundary, as the caching allocator would place
+    them), kept as `GradSet.flat`, so that a whole set can be copied at once."""
     w = WORKLOADS[name_or_workload] if isinstance(name_or_workload, str) else name_or_workload
     layout = list(w.layout)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     spiked, inf_at = _choices(seed, layout, w)
+    dt = TORCH_DTYPES[w.dtype]
+    flat_buf, views = None, None
+    if flat:
+        es = w.elem_bytes
+        offs, pos = [], 0
+        for spec in layout:
+            offs.append(pos)
+            pos += (spec.numel * es + 255) // 256 * 256
+        flat_buf = torch.zeros(pos // es, dtype=dt, device=device)
+        views = [flat_buf[o // es:o // es + spec.numel].view(spec.shape)
+                 for o, spec in zip(offs, layout)]
     tensors = []
     for i, spec in enumerate(layout):
         t = torch.randn(spec.shape, generator=gen, device=device, dtype=torch.float32)
         t.mul_(w.std * (w.spike_factor if i in spiked else 1.0))
-        tensors.append(t.to(TORCH_DTYPES[w.dtype]))
+        if views is not None:
+            views[i].copy_(t)
+            tensors.append(views[i])
+        else:
+            tensors.append(t.to(dt))
     if inf_at is not None:
         tensors[inf_at[0]].view(-1)[inf_at[1]] = float("inf")
-    return GradSet(w, tensors, [layout[i].name for i in spiked], inf_at)
+    gs = GradSet(w, tensors, [layout[i].name for i in spiked], inf_at)
+    gs.flat = flat_buf
+    return gs
 
 
 def fill_gradset_(gs: GradSet, seed: int = SEED) -> None:
