@@ -45,7 +45,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=3200)
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["gclip", "reference"], default="gclip")
-    p.add_argument("--variant", choices=["three_kernel", "persistent"], default="persistent")
+    p.add_argument("--variant", choices=["three_kernel", "persistent"], default="three_kernel")
     p.add_argument("--workload", default="andrea120m")
     p.add_argument("--pool", type=int, default=32, help="distinct gradient sets per timed run")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -353,6 +353,8 @@ def run_gclip(args):
     # per-kernel durations for the roofline (events between the launches)
     launches_per_step = 3 if args.variant == "three_kernel" else 1
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:           # torch creates the CUDA event on its first record
+        e.record(stream)
     import ctypes
     ev_handles = (ctypes.c_void_p * 4)(*[e.cuda_event for e in evs])
     L = g.load()
