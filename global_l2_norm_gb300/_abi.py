@@ -16,6 +16,7 @@ GCLIP_ERR_INVALID_ARG = 1
 GCLIP_ERR_OOM = 2
 GCLIP_ERR_CUDA = 3
 GCLIP_ERR_UNSUPPORTED = 4
+GCLIP_ERR_TOO_LARGE = 5
 # device status
 GCLIP_STATUS_OK = 0
 GCLIP_STATUS_TIMEOUT = 1
@@ -33,6 +34,8 @@ GCLIP_VARIANT_PERSISTENT = 1
 
 GCLIP_CHUNK_BYTES = 32768
 GCLIP_MAX_TENSORS = 1 << 24
+GCLIP_NOALLOC_MAX_CHUNKS = 65536
+GCLIP_NOALLOC_SCRATCH_BYTES = GCLIP_NOALLOC_MAX_CHUNKS * 8 + 256
 
 
 class clip_tensor_desc_t(ctypes.Structure):
@@ -73,6 +76,8 @@ _SIGNATURES = {
                                  ctypes.POINTER(ctypes.c_int64)]),
     "clip_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "clip_debug_barrier": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
+    "clip_grad_norm_flat_noalloc": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32,
+                                                   ctypes.c_float, ctypes.c_float, _P, _P, _P]),
 }
 
 _LIB = None

@@ -31,6 +31,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "internal.hpp"
@@ -799,5 +800,138 @@ extern "C" int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals, int64
   if (h == nullptr || extra_arrivals < 0 || timeout_ns < 0) return GCLIP_ERR_INVALID_ARG;
   h->debug_extra = extra_arrivals;
   h->timeout_ns = timeout_ns > 0 ? timeout_ns : gclip::kDefaultTimeoutNs;
+  return GCLIP_OK;
+}
+
+// ===========================================================================
+// No-allocation entry point: one contiguous buffer, scratch in a fixed array.
+
+namespace gclip {
+
+// The scratch of clip_grad_norm_flat_noalloc: the per-chunk partial sums,
+// then the result record.  Compiled into the library, so it costs every GPU
+// that loads the library GCLIP_NOALLOC_SCRATCH_BYTES until exit.
+constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(GCLIP_NOALLOC_MAX_CHUNKS) * 8;
+static_assert(kNoAllocPartialBytes + sizeof(clip_result_t) <= GCLIP_NOALLOC_SCRATCH_BYTES,
+              "record does not fit the scratch");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GCLIP_NOALLOC_SCRATCH_BYTES];
+
+// Chunk c of a single tensor at `base`, cut exactly as the host planner cuts
+// one tensor: the first chunk takes the elements before the first 16-byte
+// boundary plus a full chunk, every later chunk starts aligned.
+__device__ __forceinline__ clip_chunk_t flat_chunk(uint64_t base, int64_t numel, int32_t dtype,
+                                                   int64_t c) {
+  const int64_t es = dtype == GCLIP_F32 ? 4 : 2;
+  const int64_t per = GCLIP_CHUNK_BYTES / es;
+  const int64_t head = static_cast<int64_t>((16u - (base & 15u)) & 15u) / es;
+  const int64_t start = c == 0 ? 0 : head + c * per;
+  const int64_t want = c == 0 ? head + per : per;
+  const int64_t left = numel - start;
+  clip_chunk_t ch;
+  ch.addr = base + static_cast<uint64_t>(start * es);
+  ch.numel = static_cast<uint32_t>(left < want ? left : want);
+  ch.meta = static_cast<uint32_t>(dtype);
+  return ch;
+}
+
+__global__ void __launch_bounds__(kThreads) k_grad_norm_partial_flat(uint64_t base, int64_t numel,
+                                                                     int32_t dtype, float inv_scale,
+                                                                     float2* __restrict__ partials) {
+  __shared__ FF red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const clip_chunk_t c = flat_chunk(base, numel, dtype, blockIdx.x);
+  const FF acc = chunk_sumsq(c, inv_scale, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
+}
+
+__global__ void __launch_bounds__(kThreads) k_grad_scale_flat(uint64_t base, int64_t numel,
+                                                              int32_t dtype, int64_t n_chunks,
+                                                              const clip_result_t* res) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int decision = res->decision;
+  const float chi = res->coef_hi, clo = res->coef_lo;
+  if (!must_write(decision, chi, clo)) return;
+  const clip_chunk_t c =
+      flat_chunk(base, numel, dtype, n_chunks - 1 - static_cast<int64_t>(blockIdx.x));
+  chunk_scale(c, chi, clo);
+}
+
+}  // namespace gclip
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices];  // device address of the scratch, per device
+
+// Device address of the scratch array on `dev` (current), looked up once.
+void* noalloc_scratch(int dev) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, gclip::g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int clip_grad_norm_flat_noalloc(void* grads, int64_t numel, int32_t dtype,
+                                           float max_norm, float inv_scale, float* out_norm,
+                                           int32_t* out_nonfinite_flag, void* stream) {
+  const int es = gclip::elem_size(dtype);
+  if (es == 0 || numel < 0 || !valid_scalar(max_norm) || !valid_scalar(inv_scale))
+    return GCLIP_ERR_INVALID_ARG;
+  const uint64_t base = reinterpret_cast<uint64_t>(grads);
+  if (numel > 0 && (base == 0 || base % static_cast<uint64_t>(es) != 0))
+    return GCLIP_ERR_INVALID_ARG;
+  const int64_t per = GCLIP_CHUNK_BYTES / es;
+  const int64_t head = static_cast<int64_t>((16u - (base & 15u)) & 15u) / es;
+  // The first chunk holds head + per elements, every other chunk per.
+  if (numel > head + static_cast<int64_t>(GCLIP_NOALLOC_MAX_CHUNKS) * per)
+    return GCLIP_ERR_TOO_LARGE;
+  int64_t nc = 0;
+  if (numel > 0) nc = numel <= head + per ? 1 : 1 + (numel - head - 1) / per;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  char* scratch = static_cast<char*>(noalloc_scratch(dev));
+  if (scratch == nullptr) return GCLIP_ERR_CUDA;
+  float2* partials = reinterpret_cast<float2*>(scratch);
+  clip_result_t* record = reinterpret_cast<clip_result_t*>(scratch + gclip::kNoAllocPartialBytes);
+  const float2* cpartials = partials;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+
+  void* a2[] = {&cpartials, &nc, &max_norm, &inv_scale, &record, &out_norm, &out_nonfinite_flag};
+  if (nc == 0) {
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a2, false);
+  } else {
+    uint64_t b = base;
+    int64_t n = numel;
+    int32_t dt = dtype;
+    void* a1[] = {&b, &n, &dt, &inv_scale, &partials};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial_flat),
+                   static_cast<unsigned int>(nc), s, a1, false);
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a2, true);
+    const clip_result_t* crecord = record;
+    void* a3[] = {&b, &n, &dt, &nc, &crecord};
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale_flat),
+                     static_cast<unsigned int>(nc), s, a3, true);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
   return GCLIP_OK;
 }

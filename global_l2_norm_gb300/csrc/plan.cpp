@@ -108,6 +108,7 @@ extern "C" const char* clip_status_string(int32_t code) {
     case GCLIP_ERR_OOM: return "out of memory";
     case GCLIP_ERR_CUDA: return "CUDA error";
     case GCLIP_ERR_UNSUPPORTED: return "unsupported on this device";
+    case GCLIP_ERR_TOO_LARGE: return "larger than the fixed no-allocation scratch allows";
     default: return "unknown status";
   }
 }

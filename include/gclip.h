@@ -39,6 +39,7 @@ extern "C" {
 #define GCLIP_ERR_OOM 2          /* device or host allocation failed       */
 #define GCLIP_ERR_CUDA 3         /* a CUDA runtime call or launch failed   */
 #define GCLIP_ERR_UNSUPPORTED 4  /* the device cannot run the request      */
+#define GCLIP_ERR_TOO_LARGE 5    /* more than the fixed scratch can hold   */
 
 /* ---- values written to clip_result_t.status on the device -------------- */
 #define GCLIP_STATUS_OK 0
@@ -243,6 +244,53 @@ const char *clip_status_string(int32_t code);
  * normal operation.  Returns GCLIP_OK or GCLIP_ERR_INVALID_ARG. */
 int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals,
                        int64_t timeout_ns);
+
+/* clip_grad_norm_flat_noalloc -- the same clip for one contiguous gradient
+ * buffer, for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for the library's
+ * users.  Some callers cannot call cudaMalloc or hold a handle: code whose
+ * device memory is all owned by another allocator (a framework's caching
+ * allocator, or a fixed arena sized at start-up) and must not take memory
+ * from the driver in the middle of a run, where an allocation can fail or
+ * stall the device at an arbitrary point; and plug-in or callback interfaces
+ * that get a buffer and a stream but no create/destroy hooks in which to set
+ * up and free a handle.  This call asks for no memory from anyone: its
+ * scratch (the per-chunk partial sums and the result record) lives in one
+ * fixed array compiled into the library, GCLIP_NOALLOC_SCRATCH_BYTES long,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * grads: `numel` elements of format `dtype` in device memory of the current
+ *   device, contiguous, aligned to the element size; clipped in place exactly
+ *   as clip_grad_norm clips a handle made of this one tensor (same chunks,
+ *   same arithmetic, bit-identical results).
+ * max_norm, inv_scale, out_norm, out_nonfinite_flag, stream: as for
+ *   clip_grad_norm; the stream must belong to the current device.
+ * Limit: the buffer may span at most GCLIP_NOALLOC_MAX_CHUNKS chunks of
+ *   GCLIP_CHUNK_BYTES (2 GiB of gradients: 536,870,912 fp32 or 1,073,741,824
+ *   fp16/bf16 elements, a little less when the buffer does not start on a
+ *   16-byte boundary); a larger buffer returns GCLIP_ERR_TOO_LARGE and
+ *   nothing is enqueued.
+ * Set-up: the first call on each device looks up the device address of the
+ *   scratch array (with that device current) and may load the library's
+ *   device code there; make that first call before any stream capture.
+ * Sharing: every call, on every stream, uses the same scratch array and it
+ *   keeps the last call's contents.  Calls that overlap on the device race
+ *   with each other and give wrong results: serialise them (one stream, or
+ *   events).  Nothing needs clearing between calls, because every word of the
+ *   scratch that a call reads is first written by that call.  The record is
+ *   not readable through the handle functions; use out_norm and
+ *   out_nonfinite_flag.
+ * Returns GCLIP_OK; GCLIP_ERR_INVALID_ARG (bad dtype, negative numel, NULL or
+ *   misaligned grads with numel > 0, bad max_norm / inv_scale);
+ *   GCLIP_ERR_TOO_LARGE; GCLIP_ERR_CUDA (no current device, the scratch could
+ *   not be located, or a launch failed).  Allocates nothing. */
+#define GCLIP_NOALLOC_MAX_CHUNKS 65536
+#define GCLIP_NOALLOC_SCRATCH_BYTES (GCLIP_NOALLOC_MAX_CHUNKS * 8 + 256)
+int clip_grad_norm_flat_noalloc(void *grads, int64_t numel, int32_t dtype,
+                                float max_norm, float inv_scale,
+                                float *out_norm, int32_t *out_nonfinite_flag,
+                                void *stream);
 
 #ifdef __cplusplus
 }

@@ -177,7 +177,7 @@ def test_null_handle_calls(L):
 
 
 def test_status_strings(L):
-    for code in range(5):
+    for code in range(6):
         s = L.clip_status_string(code)
         assert s and s != b"unknown status"
     assert L.clip_status_string(99) == b"unknown status"
