@@ -45,9 +45,13 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=3200)
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["gclip", "reference"], default="gclip")
-    p.add_argument("--variant", choices=["three_kernel", "persistent"], default="three_kernel")
+    p.add_argument("--variant", choices=["split", "persistent", "split_tma", "persistent_tma"],
+                   default="split")
     p.add_argument("--workload", default="andrea120m")
     p.add_argument("--pool", type=int, default=32, help="distinct gradient sets per timed run")
+    p.add_argument("--l2-keep-mb", type=float, default=None,
+                   help="MB of the norm pass kept in L2 for the scaling pass "
+                        "(default: the library's choice)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -284,6 +288,9 @@ def run_gclip(args):
     P = max(1, min(args.pool, args.steps))
     sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
     clippers = [g.GradClipper(s.tensors, variant=args.variant) for s in sets]
+    if args.l2_keep_mb is not None:
+        for c in clippers:
+            c.set_l2_keep(int(args.l2_keep_mb * (1 << 20)))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 + (1 << 20), dtype=torch.uint8, device=dev)
 
@@ -351,7 +358,7 @@ def run_gclip(args):
     step_us = sorted(t / n * 1e3 for t, n in runs)
 
     # per-kernel durations for the roofline (events between the launches)
-    launches_per_step = 3 if args.variant == "three_kernel" else 1
+    launches_per_step = 1 if args.variant.startswith("persistent") else 2
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in evs:           # torch creates the CUDA event on its first record
         e.record(stream)
@@ -368,14 +375,15 @@ def run_gclip(args):
         for k in range(3):
             seg[k].append(evs[k].elapsed_time(evs[k + 1]))
     seg_ms = [statistics.mean(s) for s in seg]
-    if args.variant == "persistent":
-        kernel, k_bytes, k_ms = "k_clip_persistent", nbytes, seg_ms[2]
+    if args.variant.startswith("persistent"):
+        kernel = "k_clip_persistent_tma" if args.variant.endswith("tma") else "k_clip_persistent"
+        k_bytes, k_ms = nbytes, seg_ms[2]
         # the timed region is back-to-back launches of this one kernel
         k_ms = per_step_ms
     else:
-        shares = {"k_grad_norm_partial": (seg_ms[0], w.numel * w.elem_bytes),
-                  "k_grad_norm_final": (seg_ms[1], 0),
-                  "k_grad_scale": (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
+        tma = args.variant.endswith("tma")
+        shares = {("k_norm_tma" if tma else "k_grad_norm_partial"): (seg_ms[0], w.numel * w.elem_bytes),
+                  ("k_scale_tma" if tma else "k_grad_scale"): (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
         kernel = max(shares, key=lambda k: shares[k][0])
         k_ms, k_bytes = shares[kernel]
     peaks = {}
@@ -449,7 +457,7 @@ def run_gclip(args):
             "config": {
                 "workload": w.name, "description": w.description, "tensors": len(w.layout),
                 "elements": w.numel, "bytes_per_step": nbytes, "decision": decision_name,
-                "variant": args.variant, "pool": P, "parallelism": f"replicas x{world}",
+                "variant": args.variant, "pool": P, "l2_keep_mb": args.l2_keep_mb, "parallelism": f"replicas x{world}",
                 "l2": "inputs larger than L2 (one set per step, pool of distinct sets); "
                       "L2 flushed before each timed run",
                 "timing": "CUDA events around each run of back-to-back clips on the "
@@ -459,8 +467,8 @@ def run_gclip(args):
             "elements_per_s": round(w.numel * args.steps * world / (total_ms / 1e3), 1),
             "us_per_step_p10_p50_p90": [round(step_us[int(q * (len(step_us) - 1))], 2)
                                          for q in (0.1, 0.5, 0.9)],
-            "kernel_ms": {"partial": round(seg_ms[0], 5), "final": round(seg_ms[1], 5),
-                          "scale": round(seg_ms[2], 5)} if args.variant == "three_kernel"
+            "kernel_ms": {"norm": round(seg_ms[0], 5), "scale": round(seg_ms[2], 5)}
+            if args.variant.startswith("split")
             else {"persistent": round(seg_ms[2], 5)},
             "roofline": roofline,
             "clocks": clocks,

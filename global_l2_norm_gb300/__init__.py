@@ -22,19 +22,21 @@ from . import _abi
 from ._abi import (GCLIP_BF16, GCLIP_DECISION_CLIP, GCLIP_DECISION_PASS,
                    GCLIP_DECISION_SKIP, GCLIP_F16, GCLIP_F32, GCLIP_STATUS_OK,
                    GCLIP_STATUS_TIMEOUT, GCLIP_VARIANT_PERSISTENT,
-                   GCLIP_VARIANT_THREE_KERNEL, GclipError, clip_chunk_t,
+                   GCLIP_VARIANT_SPLIT, GclipError, clip_chunk_t,
                    clip_result_t, clip_tensor_desc_t, check, load)
 from ._build import build as _build_lib
 
 __all__ = ["build", "load", "GradClipper", "GclipError", "plan", "descs_for",
-           "GCLIP_F32", "GCLIP_F16", "GCLIP_BF16", "GCLIP_VARIANT_THREE_KERNEL",
+           "GCLIP_F32", "GCLIP_F16", "GCLIP_BF16", "GCLIP_VARIANT_SPLIT",
            "GCLIP_VARIANT_PERSISTENT", "GCLIP_DECISION_PASS", "GCLIP_DECISION_CLIP",
            "GCLIP_DECISION_SKIP", "GCLIP_STATUS_OK", "GCLIP_STATUS_TIMEOUT"]
 
 DTYPE_CODES = {torch.float32: GCLIP_F32, torch.float16: GCLIP_F16,
                torch.bfloat16: GCLIP_BF16}
-VARIANTS = {"three_kernel": GCLIP_VARIANT_THREE_KERNEL,
-            "persistent": GCLIP_VARIANT_PERSISTENT}
+VARIANTS = {"split": GCLIP_VARIANT_SPLIT,
+            "persistent": GCLIP_VARIANT_PERSISTENT,
+            "split_tma": _abi.GCLIP_VARIANT_SPLIT_TMA,
+            "persistent_tma": _abi.GCLIP_VARIANT_PERSISTENT_TMA}
 
 
 def build(force: bool = False) -> str:
@@ -128,6 +130,10 @@ class GradClipper:
         return int(self._lib.clip_num_chunks(self._h))
 
     @property
+    def tma_grid(self) -> int:
+        return int(self._lib.clip_tma_grid(self._h))
+
+    @property
     def persistent_grid(self) -> int:
         return int(self._lib.clip_persistent_grid(self._h))
 
@@ -140,6 +146,9 @@ class GradClipper:
 
     def reset(self, stream=None) -> None:
         check("clip_reset", self._lib.clip_reset(self._h, _stream_handle(stream, self.device)))
+
+    def set_l2_keep(self, nbytes: int) -> None:
+        check("clip_set_l2_keep", self._lib.clip_set_l2_keep(self._h, int(nbytes)))
 
     def debug_barrier(self, extra_arrivals: int, timeout_ns: int = 0) -> None:
         check("clip_debug_barrier", self._lib.clip_debug_barrier(

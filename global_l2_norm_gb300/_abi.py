@@ -29,8 +29,10 @@ GCLIP_DECISION_PASS = 0
 GCLIP_DECISION_CLIP = 1
 GCLIP_DECISION_SKIP = 2
 # variants
-GCLIP_VARIANT_THREE_KERNEL = 0
+GCLIP_VARIANT_SPLIT = 0
 GCLIP_VARIANT_PERSISTENT = 1
+GCLIP_VARIANT_SPLIT_TMA = 2
+GCLIP_VARIANT_PERSISTENT_TMA = 3
 
 GCLIP_CHUNK_BYTES = 32768
 GCLIP_MAX_TENSORS = 1 << 24
@@ -71,11 +73,13 @@ _SIGNATURES = {
     "clip_reset": (ctypes.c_int, [_P, _P]),
     "clip_num_chunks": (ctypes.c_int64, [_P]),
     "clip_persistent_grid": (ctypes.c_int32, [_P]),
+    "clip_tma_grid": (ctypes.c_int32, [_P]),
     "clip_plan": (ctypes.c_int, [ctypes.POINTER(clip_tensor_desc_t), ctypes.c_int32,
                                  ctypes.POINTER(clip_chunk_t), ctypes.c_int64,
                                  ctypes.POINTER(ctypes.c_int64)]),
     "clip_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "clip_debug_barrier": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
+    "clip_set_l2_keep": (ctypes.c_int, [_P, ctypes.c_int64]),
     "clip_grad_norm_flat_noalloc": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_float, _P, _P, _P]),
 }

@@ -44,7 +44,7 @@ constexpr int kUnroll = 8;                // 16-byte vectors in flight per threa
 constexpr long long kDefaultTimeoutNs = 1000000000LL;  // grid barrier: 1 s
 
 struct SyncWords {
-  unsigned int arrive;  // blocks that finished their partial sums this call
+  unsigned int arrive;  // blocks done with the norm pass in this call
   unsigned int gen;     // bumped once per call when the record is published
   unsigned int pad[2];
 };
@@ -234,19 +234,63 @@ __device__ __forceinline__ Span make_span(uint64_t addr, uint32_t n) {
 }
 
 // ---------------------------------------------------------------------------
+// Memory access of a chunk's vector body.  Plain: .cg loads for the norm
+// pass, streaming (.cs) loads and stores for the scaling pass.  Hinted: the
+// same accesses carry an L2 eviction policy made by createpolicy, so that the
+// norm pass can keep the chunks it reads last resident in L2 (evict_last)
+// for the scaling pass, which visits them first, and let everything else go
+// (evict_first).
+
+struct PlainMem {
+  __device__ static __forceinline__ uint4 ld_norm(const uint4* p, uint64_t) { return __ldcg(p); }
+  __device__ static __forceinline__ uint4 ld_scale(const uint4* p, uint64_t) { return __ldcs(p); }
+  __device__ static __forceinline__ void st_scale(uint4* p, uint4 v, uint64_t) { __stcs(p, v); }
+};
+
+struct HintMem {
+  __device__ static __forceinline__ uint4 ld(const uint4* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+  }
+  __device__ static __forceinline__ uint4 ld_norm(const uint4* p, uint64_t pol) { return ld(p, pol); }
+  __device__ static __forceinline__ uint4 ld_scale(const uint4* p, uint64_t pol) { return ld(p, pol); }
+  __device__ static __forceinline__ void st_scale(uint4* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+  }
+};
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------------------
 // Sum of squares of one chunk: this thread's share, in a fixed order.
 
-template <int DT>
-__device__ __forceinline__ FF chunk_sumsq_thread(uint64_t addr, uint32_t n, float s) {
+template <int DT, class M>
+__device__ __forceinline__ FF chunk_sumsq_thread(FF acc, uint64_t addr, uint32_t n, float s,
+                                                 uint64_t pol) {
   const Span sp = make_span<DT>(addr, n);
   const uint4* v = reinterpret_cast<const uint4*>(sp.body);
-  FF acc = {0.f, 0.f};
   for (uint32_t base = threadIdx.x; base < sp.nvec; base += kUnroll * kThreads) {
     uint4 buf[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t i = base + u * kThreads;
-      buf[u] = i < sp.nvec ? __ldcg(v + i) : make_uint4(0, 0, 0, 0);
+      buf[u] = i < sp.nvec ? M::ld_norm(v + i, pol) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -294,22 +338,28 @@ __device__ __forceinline__ FF block_reduce(FF v, FF* red) {
   return r;
 }
 
-__device__ __forceinline__ FF chunk_sumsq(const clip_chunk_t& c, float s, FF* red) {
-  FF acc;
+// Add this thread's share of chunk `c` to its running accumulator.
+template <class M>
+__device__ __forceinline__ FF chunk_accumulate(FF acc, const clip_chunk_t& c, float s, uint64_t pol) {
   switch (c.meta & 0xffu) {
-    case GCLIP_F32: acc = chunk_sumsq_thread<GCLIP_F32>(c.addr, c.numel, s); break;
-    case GCLIP_F16: acc = chunk_sumsq_thread<GCLIP_F16>(c.addr, c.numel, s); break;
-    default: acc = chunk_sumsq_thread<GCLIP_BF16>(c.addr, c.numel, s); break;
+    case GCLIP_F32: return chunk_sumsq_thread<GCLIP_F32, M>(acc, c.addr, c.numel, s, pol);
+    case GCLIP_F16: return chunk_sumsq_thread<GCLIP_F16, M>(acc, c.addr, c.numel, s, pol);
+    default: return chunk_sumsq_thread<GCLIP_BF16, M>(acc, c.addr, c.numel, s, pol);
   }
-  return block_reduce(acc, red);
+}
+
+// The sum of squares of one chunk, valid in thread 0.
+template <class M>
+__device__ __forceinline__ FF chunk_sumsq(const clip_chunk_t& c, float s, FF* red, uint64_t pol) {
+  return block_reduce(chunk_accumulate<M>(FF{0.f, 0.f}, c, s, pol), red);
 }
 
 // ---------------------------------------------------------------------------
-// Scaling of one chunk in place.  Loads and stores are marked streaming
-// (evict-first): this data is not read again.
+// Scaling of one chunk in place.
 
-template <int DT>
-__device__ __forceinline__ void chunk_scale_thread(uint64_t addr, uint32_t n, float chi, float clo) {
+template <int DT, class M>
+__device__ __forceinline__ void chunk_scale_thread(uint64_t addr, uint32_t n, float chi, float clo,
+                                                   uint64_t pol) {
   const Span sp = make_span<DT>(addr, n);
   uint4* v = reinterpret_cast<uint4*>(sp.body);
   for (uint32_t base = threadIdx.x; base < sp.nvec; base += kUnroll * kThreads) {
@@ -317,12 +367,12 @@ __device__ __forceinline__ void chunk_scale_thread(uint64_t addr, uint32_t n, fl
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t i = base + u * kThreads;
-      buf[u] = i < sp.nvec ? __ldcs(v + i) : make_uint4(0, 0, 0, 0);
+      buf[u] = i < sp.nvec ? M::ld_scale(v + i, pol) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t i = base + u * kThreads;
-      if (i < sp.nvec) __stcs(v + i, Fmt<DT>::scale(buf[u], chi, clo));
+      if (i < sp.nvec) M::st_scale(v + i, Fmt<DT>::scale(buf[u], chi, clo), pol);
     }
   }
   constexpr uint32_t B = Fmt<DT>::kBytes;
@@ -336,11 +386,12 @@ __device__ __forceinline__ void chunk_scale_thread(uint64_t addr, uint32_t n, fl
   }
 }
 
-__device__ __forceinline__ void chunk_scale(const clip_chunk_t& c, float chi, float clo) {
+template <class M>
+__device__ __forceinline__ void chunk_scale(const clip_chunk_t& c, float chi, float clo, uint64_t pol) {
   switch (c.meta & 0xffu) {
-    case GCLIP_F32: chunk_scale_thread<GCLIP_F32>(c.addr, c.numel, chi, clo); break;
-    case GCLIP_F16: chunk_scale_thread<GCLIP_F16>(c.addr, c.numel, chi, clo); break;
-    default: chunk_scale_thread<GCLIP_BF16>(c.addr, c.numel, chi, clo); break;
+    case GCLIP_F32: chunk_scale_thread<GCLIP_F32, M>(c.addr, c.numel, chi, clo, pol); break;
+    case GCLIP_F16: chunk_scale_thread<GCLIP_F16, M>(c.addr, c.numel, chi, clo, pol); break;
+    default: chunk_scale_thread<GCLIP_BF16, M>(c.addr, c.numel, chi, clo, pol); break;
   }
 }
 
@@ -349,8 +400,9 @@ __device__ __forceinline__ bool must_write(int decision, float chi, float clo) {
 }
 
 // ---------------------------------------------------------------------------
-// Final reduction over the per-chunk partial sums, square root and decision.
-// Runs on one block of kThreads threads; the record is written by thread 0.
+// Final reduction over partial sums, square root and decision.  Runs on one
+// block of kThreads threads: thread t sums entries t, t + kThreads, ... in
+// increasing order, then the fixed block tree; thread 0 writes the record.
 //
 // The decision is taken in double from the float-float sum: S = hi + lo is
 // exact in double, norm = sqrt(S) and max_norm / norm are IEEE double
@@ -409,19 +461,78 @@ __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max
 }
 
 // ---------------------------------------------------------------------------
-// Three-kernel variant.
+// The norm pass of the handle-based clip, shared by both variants.
+//
+// A grid of G blocks (G fixed per handle: the co-resident count of the
+// single-launch kernel, at most the number of chunks).  Block b takes chunks
+// b, b + G, b + 2G, ...; each of its threads keeps one float-float
+// accumulator over its share of all those chunks, in that order, and the
+// block tree combines the threads once at the end.  The block sum goes to
+// block_sums[b]; the block that arrives last reduces the G block sums in
+// fixed order (final_reduce) and publishes the record.  Which block arrives
+// last depends on timing; the arithmetic does not.
 
-__global__ void __launch_bounds__(kThreads) k_grad_norm_partial(const clip_chunk_t* __restrict__ chunks,
-                                                                float inv_scale,
-                                                                float2* __restrict__ partials) {
-  __shared__ FF red[kWarps];
-  // Let the dependent final-reduce launch be scheduled while this grid runs.
-  asm volatile("griddepcontrol.launch_dependents;");
-  const clip_chunk_t c = chunks[blockIdx.x];
-  const FF acc = chunk_sumsq(c, inv_scale, red);
-  if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
+struct NormArgs {
+  const clip_chunk_t* chunks;
+  int64_t n_chunks;
+  float2* block_sums;     // G entries
+  unsigned int* arrive;   // blocks done with the norm pass in this call
+  unsigned int expected;  // G, plus the test hook's extra arrivals
+  float max_norm;
+  float inv_scale;
+  clip_result_t* res;
+  float* out_norm;
+  int32_t* out_flag;
+  int64_t keep_from;      // chunks from here on are read with evict_last
+};
+
+__device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
+  const uint64_t pol_first = policy_evict_first();
+  const uint64_t pol_last = policy_evict_last();
+  FF acc = {0.f, 0.f};
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const clip_chunk_t ch = a.chunks[c];
+    acc = chunk_accumulate<HintMem>(acc, ch, a.inv_scale, c >= a.keep_from ? pol_last : pol_first);
+  }
+  return block_reduce(acc, red);
 }
 
+// Publish this block's sum; returns true (in every thread) in the block that
+// arrived last, after it has written the record.
+__device__ __forceinline__ bool norm_arrive(const NormArgs& a, FF bsum, FF* red, int* s_flag) {
+  if (threadIdx.x == 0) {
+    a.block_sums[blockIdx.x] = make_float2(bsum.hi, bsum.lo);
+    __threadfence();
+    const unsigned int t = atomicAdd(a.arrive, 1u);
+    *s_flag = (t + 1u == a.expected);
+  }
+  __syncthreads();
+  if (!*s_flag) return false;
+  __threadfence();
+  final_reduce(a.block_sums, gridDim.x, a.max_norm, a.inv_scale, a.res, a.out_norm, a.out_flag,
+               red);
+  if (threadIdx.x == 0) {
+    *a.arrive = 0u;  // every block has arrived: rearm for the next call
+    __threadfence();
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Split variant: the norm pass (with the final reduction in the last block)
+// and the scaling pass as two launches.
+
+__global__ void __launch_bounds__(kThreads) k_grad_norm_partial(const NormArgs a) {
+  __shared__ FF red[kWarps];
+  __shared__ int s_flag;
+  // Let the dependent scaling launch be scheduled while this grid runs.
+  asm volatile("griddepcontrol.launch_dependents;");
+  const FF bsum = block_norm_pass(a, red);
+  norm_arrive(a, bsum, red, &s_flag);
+}
+
+// One block of the final reduction alone: used when there are no chunks and
+// by the no-allocation entry point.
 __global__ void __launch_bounds__(kThreads) k_grad_norm_final(const float2* __restrict__ partials,
                                                               int64_t n_chunks, float max_norm,
                                                               float inv_scale, clip_result_t* res,
@@ -439,10 +550,9 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __r
   const int decision = res->decision;
   const float chi = res->coef_hi, clo = res->coef_lo;
   if (!must_write(decision, chi, clo)) return;
-  // Highest chunks first: the partial pass read them last, so they are the
-  // ones most likely still held in L2.
+  // Highest chunks first: the norm pass read them last and kept them in L2.
   const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
-  chunk_scale(c, chi, clo);
+  chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
 }
 
 // ---------------------------------------------------------------------------
@@ -460,41 +570,23 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-__global__ void __launch_bounds__(kThreads) k_clip_persistent(
-    const clip_chunk_t* __restrict__ chunks, int64_t n_chunks, float max_norm, float inv_scale,
-    float2* __restrict__ partials, clip_result_t* res, float* out_norm, int32_t* out_flag,
-    SyncWords* sync, unsigned int expected, long long timeout_ns) {
+__global__ void __launch_bounds__(kThreads) k_clip_persistent(const NormArgs a, SyncWords* sync,
+                                                              long long timeout_ns) {
   __shared__ FF red[kWarps];
   __shared__ unsigned int s_gen0;
-  __shared__ int s_last, s_go;
+  __shared__ int s_flag, s_go;
 
-  // The generation before this call; it changes only after every block has
-  // arrived, so each block reads the same value here.
+  // The generation before this call.  It is bumped only after every block
+  // has arrived, so each block reads the same value here.
   if (threadIdx.x == 0) s_gen0 = *reinterpret_cast<volatile unsigned int*>(&sync->gen);
 
-  // Phase 1: per-chunk partial sums, chunks strided over the grid.
-  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-    const clip_chunk_t ch = chunks[c];
-    const FF acc = chunk_sumsq(ch, inv_scale, red);
-    if (threadIdx.x == 0) partials[c] = make_float2(acc.hi, acc.lo);
-  }
+  // Phase 1: the norm pass; the block that arrives last publishes the record.
+  const FF bsum = block_norm_pass(a, red);
+  const bool published = norm_arrive(a, bsum, red, &s_flag);
 
-  // Arrival: the block that takes the last ticket reduces.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int t = atomicAdd(&sync->arrive, 1u);
-    s_last = (t + 1u == expected);
-  }
-  __syncthreads();
-
-  if (s_last) {
-    __threadfence();
-    final_reduce(partials, n_chunks, max_norm, inv_scale, res, out_norm, out_flag, red);
-    __syncthreads();
+  if (published) {
     if (threadIdx.x == 0) {
-      sync->arrive = 0u;  // every block has arrived: safe to rearm
-      __threadfence();
-      atomicAdd(&sync->gen, 1u);
+      atomicAdd(&sync->gen, 1u);  // release: the record was fenced above
       s_go = 1;
     }
   } else if (threadIdx.x == 0) {
@@ -504,7 +596,7 @@ __global__ void __launch_bounds__(kThreads) k_clip_persistent(
     int ok = 1;
     while (ld_acquire(&sync->gen) == s_gen0) {
       if (static_cast<long long>(globaltimer() - t0) > timeout_ns) {
-        atomicExch(&res->status, GCLIP_STATUS_TIMEOUT);
+        atomicExch(&a.res->status, GCLIP_STATUS_TIMEOUT);
         ok = 0;
         break;
       }
@@ -517,14 +609,433 @@ __global__ void __launch_bounds__(kThreads) k_clip_persistent(
   __syncthreads();
   if (!s_go) return;
 
-  const int decision = __ldcg(&res->decision);
-  const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
+  const int decision = __ldcg(&a.res->decision);
+  const float chi = __ldcg(&a.res->coef_hi), clo = __ldcg(&a.res->coef_lo);
   if (!must_write(decision, chi, clo)) return;
   // Phase 2: the same chunks in reverse order, most recently read first.
-  for (int64_t k = blockIdx.x; k < n_chunks; k += gridDim.x) {
-    const clip_chunk_t ch = chunks[n_chunks - 1 - k];
-    chunk_scale(ch, chi, clo);
+  const uint64_t pol = policy_evict_first();
+  for (int64_t k = blockIdx.x; k < a.n_chunks; k += gridDim.x) {
+    const clip_chunk_t ch = a.chunks[a.n_chunks - 1 - k];
+    chunk_scale<HintMem>(ch, chi, clo, pol);
   }
+}
+
+// ===========================================================================
+// TMA engine: the same two passes with bulk copies through a ring of shared
+// memory stages.  Two blocks per SM; each block's issuing thread keeps up to
+// kStages chunk bodies (the 16-byte-aligned run of each chunk, at most
+// GCLIP_CHUNK_BYTES) in flight with cp.async.bulk, each stage completing on
+// its own mbarrier; all 256 threads consume a stage from shared memory with
+// the same element-to-thread mapping as the register engine.  The scaling
+// pass rewrites the stage in shared memory and stores it back with a bulk
+// store.  Every wait is bounded: on timeout the block records
+// GCLIP_STATUS_TIMEOUT, waits (bounded) for the copies it still has in
+// flight, and returns without writing gradients.
+
+constexpr int kStages = 3;
+constexpr uint32_t kStageBytes = GCLIP_CHUNK_BYTES;
+constexpr size_t kTmaSmem = static_cast<size_t>(kStages) * kStageBytes + kStages * sizeof(uint64_t);
+constexpr long long kRingTimeoutNs = 1000000000LL;  // one chunk copy: 1 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on one phase, by thread 0 alone; true if it completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long timeout_ns) {
+  const unsigned long long t0 = globaltimer();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0 && static_cast<long long>(globaltimer() - t0) > timeout_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, uint64_t src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(uint64_t dst, const void* src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(smem_addr(src)), "r"(bytes), "l"(pol)
+               : "memory");
+}
+
+// Close this thread's bulk-store group (possibly empty), one per chunk.
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Bulk stores of this thread: at most N groups may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The aligned vector body of a chunk: device address and byte count.
+__device__ __forceinline__ void chunk_body(const clip_chunk_t& c, uint64_t& addr, uint32_t& bytes) {
+  const uint32_t es = (c.meta & 0xffu) == GCLIP_F32 ? 4u : 2u;
+  const uint32_t per = 16u / es;
+  const uint32_t head = min(c.numel, static_cast<uint32_t>(((16u - (c.addr & 15u)) & 15u) / es));
+  addr = c.addr + static_cast<uint64_t>(head) * es;
+  bytes = (c.numel - head) / per * 16u;
+}
+
+// Thread 0: start the copy of chunk `c` into stage `st`.
+__device__ __forceinline__ void ring_issue(uint8_t* st, uint64_t* bar, const clip_chunk_t& c, uint64_t pol) {
+  uint64_t src;
+  uint32_t bytes;
+  chunk_body(c, src, bytes);
+  if (bytes) {
+    mbar_expect_tx(bar, bytes);
+    bulk_load(st, src, bytes, bar, pol);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+// The ring's shared memory: kStages data stages, then kStages mbarriers.
+struct Ring {
+  uint8_t* data;
+  uint64_t* full;
+  __device__ uint8_t* stage(int s) const { return data + static_cast<size_t>(s) * kStageBytes; }
+};
+
+__device__ __forceinline__ Ring ring_setup(uint8_t* smem) {
+  Ring r;
+  r.data = smem;
+  r.full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kStages) * kStageBytes);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&r.full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  return r;
+}
+
+// Stage k % kStages holds the k-th chunk of this block's sequence; `phase`
+// keeps, per stage, the parity of its next phase.  Every thread keeps the
+// same copy and flips a bit for each chunk it consumes.
+__device__ __forceinline__ uint32_t take_parity(uint32_t& phase, int s) {
+  const uint32_t p = (phase >> s) & 1u;
+  phase ^= 1u << s;
+  return p;
+}
+
+// Thread 0: wait, bounded, for the copies of chunks k .. issued - 1.
+__device__ __forceinline__ void ring_drain(const Ring& r, int64_t k, int64_t issued, uint32_t phase,
+                                           long long timeout_ns) {
+  for (int64_t j = k; j < issued; ++j) {
+    const int s = static_cast<int>(j % kStages);
+    mbar_wait_bounded(&r.full[s], take_parity(phase, s), timeout_ns);
+  }
+}
+
+// Wait for chunk k to land.  Every thread waits for itself (the wait also
+// makes the stage's contents visible to it).  A thread that gives up records
+// the status and raises the block's abort flag, which the block reads after
+// its next barrier.
+__device__ __forceinline__ bool ring_wait(const Ring& r, int64_t k, uint32_t& phase, clip_result_t* res,
+                                          volatile int* s_abort) {
+  const int s = static_cast<int>(k % kStages);
+  const uint32_t parity = take_parity(phase, s);
+  if (mbar_wait_bounded(&r.full[s], parity, kRingTimeoutNs)) return true;
+  atomicExch(&res->status, GCLIP_STATUS_TIMEOUT);
+  *s_abort = 1;
+  return false;
+}
+
+// After the barrier that follows chunk k: if any thread gave up, thread 0
+// waits (bounded) for the copies that may still be in flight, chunk k's
+// included, and the block returns.  `phase` is thread 0's, already advanced
+// past chunk k, so chunk k's bit is turned back first.
+__device__ __forceinline__ bool ring_aborted(const Ring& r, int64_t k, int64_t issued, uint32_t phase,
+                                             volatile int* s_abort) {
+  if (!*s_abort) return false;
+  if (threadIdx.x == 0)
+    ring_drain(r, k, issued, phase ^ (1u << static_cast<int>(k % kStages)), kRingTimeoutNs / 10);
+  return true;
+}
+
+// This thread's share of one staged chunk, added to four independent
+// accumulators (vector j of the thread's share goes to acc[j % 4]) so that
+// four float-float chains run side by side; head and tail scalars go to
+// acc[0].  The order is fixed, so the result is deterministic.
+template <int DT>
+__device__ __forceinline__ void stage_sumsq(FF (&acc)[4], const uint8_t* st, const clip_chunk_t& c,
+                                            float s) {
+  const Span sp = make_span<DT>(c.addr, c.numel);
+  const uint4* v = reinterpret_cast<const uint4*>(st);
+  uint32_t i = threadIdx.x;
+  for (; i + 3 * kThreads < sp.nvec; i += 4 * kThreads) {
+    const uint4 v0 = v[i], v1 = v[i + kThreads], v2 = v[i + 2 * kThreads], v3 = v[i + 3 * kThreads];
+    acc[0] = ff_add_f(acc[0], Fmt<DT>::sumsq(v0, s));
+    acc[1] = ff_add_f(acc[1], Fmt<DT>::sumsq(v1, s));
+    acc[2] = ff_add_f(acc[2], Fmt<DT>::sumsq(v2, s));
+    acc[3] = ff_add_f(acc[3], Fmt<DT>::sumsq(v3, s));
+  }
+  // fewer than four vectors left: constant indices keep acc in registers
+  if (i < sp.nvec) acc[0] = ff_add_f(acc[0], Fmt<DT>::sumsq(v[i], s));
+  if (i + kThreads < sp.nvec) acc[1] = ff_add_f(acc[1], Fmt<DT>::sumsq(v[i + kThreads], s));
+  if (i + 2 * kThreads < sp.nvec) acc[2] = ff_add_f(acc[2], Fmt<DT>::sumsq(v[i + 2 * kThreads], s));
+  constexpr uint32_t B = Fmt<DT>::kBytes;
+  if (threadIdx.x < sp.head) {
+    const float y = __fmul_rn(Fmt<DT>::load1(c.addr + threadIdx.x * B), s);
+    acc[0] = ff_add_f(acc[0], __fmul_rn(y, y));
+  }
+  if (threadIdx.x < sp.ntail) {
+    const float y =
+        __fmul_rn(Fmt<DT>::load1(c.addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B), s);
+    acc[0] = ff_add_f(acc[0], __fmul_rn(y, y));
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void stage_scale(uint8_t* st, const clip_chunk_t& c, float chi, float clo) {
+  const Span sp = make_span<DT>(c.addr, c.numel);
+  uint4* v = reinterpret_cast<uint4*>(st);
+  for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) v[i] = Fmt<DT>::scale(v[i], chi, clo);
+  constexpr uint32_t B = Fmt<DT>::kBytes;
+  if (threadIdx.x < sp.head) {
+    const uint64_t a = c.addr + threadIdx.x * B;
+    Fmt<DT>::store1(a, Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(a), chi, clo));
+  }
+  if (threadIdx.x < sp.ntail) {
+    const uint64_t a = c.addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B;
+    Fmt<DT>::store1(a, Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(a), chi, clo));
+  }
+}
+
+// Chunk k of this block's sequence in the norm pass (increasing) and in the
+// scaling pass (decreasing, most recently read first).
+__device__ __forceinline__ int64_t norm_chunk(int64_t k) { return blockIdx.x + k * gridDim.x; }
+__device__ __forceinline__ int64_t scale_chunk(int64_t n, int64_t k) {
+  return n - 1 - (blockIdx.x + k * gridDim.x);
+}
+__device__ __forceinline__ int64_t my_count(int64_t n) {
+  return blockIdx.x < n ? (n - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+}
+
+// Norm pass through the ring; the block sum is valid in thread 0.  Returns
+// false (uniformly) if a copy timed out; no copy is then in flight.
+__device__ bool tma_norm_pass(const NormArgs& a, const Ring& r, uint32_t& phase, FF* red,
+                              volatile int* s_abort, FF* out) {
+  const int64_t mine = my_count(a.n_chunks);
+  const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
+  int64_t issued = 0;
+  if (threadIdx.x == 0) {
+    for (; issued < kStages && issued < mine; ++issued) {
+      const int64_t c = norm_chunk(issued);
+      ring_issue(r.stage(static_cast<int>(issued)), &r.full[issued], a.chunks[c],
+                 c >= a.keep_from ? pol_last : pol_first);
+    }
+  }
+  FF acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  for (int64_t k = 0; k < mine; ++k) {
+    const int s = static_cast<int>(k % kStages);
+    if (ring_wait(r, k, phase, a.res, s_abort)) {
+      const clip_chunk_t ch = a.chunks[norm_chunk(k)];
+      switch (ch.meta & 0xffu) {
+        case GCLIP_F32: stage_sumsq<GCLIP_F32>(acc, r.stage(s), ch, a.inv_scale); break;
+        case GCLIP_F16: stage_sumsq<GCLIP_F16>(acc, r.stage(s), ch, a.inv_scale); break;
+        default: stage_sumsq<GCLIP_BF16>(acc, r.stage(s), ch, a.inv_scale); break;
+      }
+    }
+    __syncthreads();
+    if (ring_aborted(r, k, issued, phase, s_abort)) return false;
+    if (threadIdx.x == 0 && issued < mine) {
+      const int64_t c = norm_chunk(issued);
+      fence_proxy_async();
+      ring_issue(r.stage(s), &r.full[s], a.chunks[c], c >= a.keep_from ? pol_last : pol_first);
+      ++issued;
+    }
+  }
+  *out = block_reduce(ff_add(ff_add(acc[0], acc[1]), ff_add(acc[2], acc[3])), red);
+  return true;
+}
+
+// Thread 0: prefetch the first kStages - 1 chunks of the scaling pass.
+__device__ __forceinline__ int64_t tma_scale_prefetch(const clip_chunk_t* chunks, int64_t n, const Ring& r,
+                                                      uint64_t pol) {
+  const int64_t mine = my_count(n);
+  int64_t issued = 0;
+  fence_proxy_async();
+  for (; issued < kStages - 1 && issued < mine; ++issued)
+    ring_issue(r.stage(static_cast<int>(issued)), &r.full[issued], chunks[scale_chunk(n, issued)], pol);
+  return issued;
+}
+
+// Scaling pass through the ring, after tma_scale_prefetch (thread 0's
+// `issued` counts the chunks it has started).  Returns false (uniformly) if a
+// copy timed out; no copy or store is then in flight.
+__device__ bool tma_scale_pass(const clip_chunk_t* chunks, int64_t n, const Ring& r, uint32_t& phase,
+                               int64_t issued, float chi, float clo, clip_result_t* res,
+                               volatile int* s_abort) {
+  const int64_t mine = my_count(n);
+  const uint64_t pol = policy_evict_first();
+  for (int64_t k = 0; k < mine; ++k) {
+    const int s = static_cast<int>(k % kStages);
+    const clip_chunk_t ch = chunks[scale_chunk(n, k)];
+    if (ring_wait(r, k, phase, res, s_abort)) {
+      switch (ch.meta & 0xffu) {
+        case GCLIP_F32: stage_scale<GCLIP_F32>(r.stage(s), ch, chi, clo); break;
+        case GCLIP_F16: stage_scale<GCLIP_F16>(r.stage(s), ch, chi, clo); break;
+        default: stage_scale<GCLIP_BF16>(r.stage(s), ch, chi, clo); break;
+      }
+    }
+    fence_proxy_async();  // this thread's shared-memory writes, visible to the bulk store
+    __syncthreads();
+    if (ring_aborted(r, k, issued, phase, s_abort)) {
+      if (threadIdx.x == 0) bulk_wait_all();
+      return false;
+    }
+    if (threadIdx.x == 0) {
+      uint64_t dst;
+      uint32_t bytes;
+      chunk_body(ch, dst, bytes);
+      if (bytes) bulk_store(dst, r.stage(s), bytes, pol);
+      bulk_commit();
+      if (issued < mine) {
+        // The stage of chunk `issued` last held chunk k - 1, whose store
+        // group was committed one iteration ago: wait until at most the
+        // newest group (chunk k's) is still reading shared memory.
+        bulk_wait_read<1>();
+        const int ns = static_cast<int>(issued % kStages);
+        ring_issue(r.stage(ns), &r.full[ns], chunks[scale_chunk(n, issued)], pol);
+        ++issued;
+      }
+    }
+  }
+  if (threadIdx.x == 0) bulk_wait_all();
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_norm_tma(const NormArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ FF red[kWarps];
+  __shared__ int s_abort, s_flag;
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) s_abort = 0;
+  const Ring r = ring_setup(smem);
+  uint32_t phase = 0;
+  FF bsum;
+  // A block whose copy timed out still arrives, with a NaN sum, so that the
+  // record is published and says SKIP.
+  if (!tma_norm_pass(a, r, phase, red, &s_abort, &bsum) && threadIdx.x == 0)
+    bsum = FF{__int_as_float(0x7fc00000), 0.f};
+  norm_arrive(a, bsum, red, &s_flag);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_scale_tma(const clip_chunk_t* __restrict__ chunks, int64_t n,
+                                                           clip_result_t* res) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort, s_go;
+  if (threadIdx.x == 0) s_abort = 0;
+  const Ring r = ring_setup(smem);
+  uint32_t phase = 0;
+  // The gradients are not written by the norm pass, so the first chunks can
+  // be fetched before the record exists; they are most likely in L2.
+  int64_t issued = 0;
+  if (threadIdx.x == 0) issued = tma_scale_prefetch(chunks, n, r, policy_evict_first());
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int decision = __ldcg(&res->decision);
+  const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
+  if (threadIdx.x == 0) s_go = must_write(decision, chi, clo) ? 1 : 0;
+  __syncthreads();
+  if (!s_go) {
+    // Nothing to write: let the prefetched copies land before leaving.
+    if (threadIdx.x == 0) ring_drain(r, 0, issued, phase, kRingTimeoutNs);
+    return;
+  }
+  tma_scale_pass(chunks, n, r, phase, issued, chi, clo, res, &s_abort);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_clip_persistent_tma(const NormArgs a, SyncWords* sync,
+                                                                     long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ FF red[kWarps];
+  __shared__ unsigned int s_gen0;
+  __shared__ int s_abort, s_flag, s_go;
+  if (threadIdx.x == 0) {
+    s_gen0 = *reinterpret_cast<volatile unsigned int*>(&sync->gen);
+    s_abort = 0;
+  }
+  const Ring r = ring_setup(smem);
+  uint32_t phase = 0;
+  FF bsum;
+  const bool ok = tma_norm_pass(a, r, phase, red, &s_abort, &bsum);
+  // A block whose copy timed out still arrives, with a NaN sum (so the clip
+  // is skipped), to keep the others from waiting for it.
+  if (!ok && threadIdx.x == 0) bsum = FF{__int_as_float(0x7fc00000), 0.f};
+  const bool published = norm_arrive(a, bsum, red, &s_flag);
+
+  // Speculative prefetch of the scaling pass while the record is pending.
+  int64_t issued = 0;
+  if (threadIdx.x == 0 && ok) issued = tma_scale_prefetch(a.chunks, a.n_chunks, r, policy_evict_first());
+
+  if (published) {
+    if (threadIdx.x == 0) {
+      atomicAdd(&sync->gen, 1u);
+      s_go = 1;
+    }
+  } else if (threadIdx.x == 0) {
+    const unsigned long long t0 = globaltimer();
+    unsigned int ns = 32;
+    int go = 1;
+    while (ld_acquire(&sync->gen) == s_gen0) {
+      if (static_cast<long long>(globaltimer() - t0) > timeout_ns) {
+        atomicExch(&a.res->status, GCLIP_STATUS_TIMEOUT);
+        go = 0;
+        break;
+      }
+      __nanosleep(ns);
+      if (ns < 1024) ns <<= 1;
+    }
+    __threadfence();
+    s_go = go;
+  }
+  __syncthreads();
+  const int decision = __ldcg(&a.res->decision);
+  const float chi = __ldcg(&a.res->coef_hi), clo = __ldcg(&a.res->coef_lo);
+  if (!ok || !s_go || !must_write(decision, chi, clo)) {
+    if (threadIdx.x == 0) ring_drain(r, 0, issued, phase, kRingTimeoutNs);
+    return;
+  }
+  tma_scale_pass(a.chunks, a.n_chunks, r, phase, issued, chi, clo, a.res, &s_abort);
 }
 
 }  // namespace gclip
@@ -537,14 +1048,17 @@ using gclip::SyncWords;
 struct gclip_handle {
   int device;
   int64_t n_chunks;
+  int64_t keep_from;         // first chunk the norm pass reads with evict_last
+  int64_t l2_bytes;          // L2 size of the device
   int32_t variant;
-  int32_t grid_persistent;
+  int32_t grid_persistent;   // blocks of the register engine (co-resident)
+  int32_t grid_tma;          // blocks of the TMA engine (co-resident)
   int32_t coop;
   int32_t debug_extra;
   long long timeout_ns;
   void* arena;
   clip_chunk_t* d_chunks;
-  float2* d_partials;
+  float2* d_partials;        // one entry per block of the norm pass (G)
   clip_result_t* d_result;
   SyncWords* d_sync;
 };
@@ -572,11 +1086,36 @@ struct DeviceGuard {
 
 bool valid_scalar(float v) { return std::isfinite(v) && v > 0.0f; }
 
-cudaError_t launch_pdl(const void* fn, unsigned int grid, cudaStream_t s, void** args, bool pdl) {
+// The norm pass marks its last `bytes` (rounded to whole chunks) evict_last
+// in L2, for the scaling pass to find there.
+void set_keep(gclip_handle* h, int64_t bytes) {
+  const int64_t k = bytes / GCLIP_CHUNK_BYTES;
+  h->keep_from = k >= h->n_chunks ? 0 : h->n_chunks - k;
+}
+
+gclip::NormArgs norm_args(gclip_handle* h, int32_t grid, float max_norm, float inv_scale,
+                          float* out_norm, int32_t* out_flag, unsigned int extra) {
+  gclip::NormArgs a;
+  a.chunks = h->d_chunks;
+  a.n_chunks = h->n_chunks;
+  a.block_sums = h->d_partials;
+  a.arrive = &h->d_sync->arrive;
+  a.expected = static_cast<unsigned int>(grid) + extra;
+  a.max_norm = max_norm;
+  a.inv_scale = inv_scale;
+  a.res = h->d_result;
+  a.out_norm = out_norm;
+  a.out_flag = out_flag;
+  a.keep_from = h->keep_from;
+  return a;
+}
+
+cudaError_t launch_pdl(const void* fn, unsigned int grid, cudaStream_t s, void** args, bool pdl,
+                       size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(gclip::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -601,10 +1140,12 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
     return GCLIP_ERR_CUDA;
   }
   h->n_chunks = static_cast<int64_t>(chunks.size());
-  h->variant = GCLIP_VARIANT_THREE_KERNEL;
+  h->variant = GCLIP_VARIANT_SPLIT;
   h->timeout_ns = gclip::kDefaultTimeoutNs;
 
   const size_t n = chunks.size();
+  // G, the norm pass's grid, is known only after the occupancy query below;
+  // it is at most the number of chunks, so size the block sums for that.
   const size_t off_chunks = 0;
   const size_t off_partials = round_up(off_chunks + n * sizeof(clip_chunk_t), 256);
   const size_t off_result = round_up(off_partials + n * sizeof(float2), 256);
@@ -622,15 +1163,26 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   h->d_result = reinterpret_cast<clip_result_t*>(base + off_result);
   h->d_sync = reinterpret_cast<SyncWords*>(base + off_sync);
 
-  int sms = 0, per_sm = 0, coop = 0;
+  int sms = 0, per_sm = 0, coop = 0, l2 = 0;
   e = cudaMemset(h->arena, 0, total);
   if (e == cudaSuccess && n > 0)
     e = cudaMemcpy(h->d_chunks, chunks.data(), n * sizeof(clip_chunk_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gclip::k_clip_persistent,
                                                       gclip::kThreads, 0);
+  int per_sm_tma = 0;
+  for (const void* fn : {reinterpret_cast<const void*>(gclip::k_norm_tma),
+                         reinterpret_cast<const void*>(gclip::k_scale_tma),
+                         reinterpret_cast<const void*>(gclip::k_clip_persistent_tma)})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(gclip::kTmaSmem));
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tma, gclip::k_clip_persistent_tma,
+                                                      gclip::kThreads, gclip::kTmaSmem);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -638,8 +1190,12 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
     delete h;
     return GCLIP_ERR_CUDA;
   }
+  h->l2_bytes = l2;
+  set_keep(h, static_cast<int64_t>(l2) / 2);
   const int64_t resident = static_cast<int64_t>(sms) * per_sm;
   h->grid_persistent = static_cast<int32_t>(resident < h->n_chunks ? resident : h->n_chunks);
+  const int64_t resident_tma = static_cast<int64_t>(sms) * per_sm_tma;
+  h->grid_tma = static_cast<int32_t>(resident_tma < h->n_chunks ? resident_tma : h->n_chunks);
   h->coop = coop;
   *out = h;
   return GCLIP_OK;
@@ -662,40 +1218,66 @@ int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
   mark(0);
   if (nc == 0) {
     mark(1);
+    mark(2);
     void* args[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm, &out_flag};
     if (e == cudaSuccess)
       e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, args, false);
-    mark(2);
-  } else if (h->variant == GCLIP_VARIANT_THREE_KERNEL) {
-    const clip_chunk_t* chunks = h->d_chunks;
-    float2* wpartials = h->d_partials;
-    void* a1[] = {&chunks, &inv_scale, &wpartials};
+  } else if (h->variant == GCLIP_VARIANT_SPLIT) {
+    gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag, 0);
+    void* a1[] = {&a};
     if (e == cudaSuccess)
       e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial),
-                     static_cast<unsigned int>(nc), s, a1, false);
+                     static_cast<unsigned int>(h->grid_persistent), s, a1, false);
     mark(1);
-    void* a2[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm, &out_flag};
-    if (e == cudaSuccess)
-      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a2, pdl);
     mark(2);
+    const clip_chunk_t* chunks = h->d_chunks;
     const clip_result_t* cres = h->d_result;
     void* a3[] = {&chunks, &nc, &cres};
     if (e == cudaSuccess)
       e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale),
                      static_cast<unsigned int>(nc), s, a3, pdl);
-  } else {
+  } else if (h->variant == GCLIP_VARIANT_SPLIT_TMA) {
+    gclip::NormArgs a = norm_args(h, h->grid_tma, max_norm, inv_scale, out_norm, out_flag, 0);
+    void* a1[] = {&a};
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_norm_tma),
+                     static_cast<unsigned int>(h->grid_tma), s, a1, false, gclip::kTmaSmem);
     mark(1);
     mark(2);
     const clip_chunk_t* chunks = h->d_chunks;
-    float2* wpartials = h->d_partials;
-    unsigned int expected =
-        static_cast<unsigned int>(h->grid_persistent) + static_cast<unsigned int>(h->debug_extra);
+    clip_result_t* res = h->d_result;
+    void* a3[] = {&chunks, &nc, &res};
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_scale_tma),
+                     static_cast<unsigned int>(h->grid_tma), s, a3, pdl, gclip::kTmaSmem);
+  } else if (h->variant == GCLIP_VARIANT_PERSISTENT_TMA) {
+    mark(1);
+    mark(2);
+    gclip::NormArgs a = norm_args(h, h->grid_tma, max_norm, inv_scale, out_norm, out_flag,
+                                  static_cast<unsigned int>(h->debug_extra));
     long long tmo = h->timeout_ns;
     if (e == cudaSuccess && h->debug_extra > 0)
       e = cudaMemsetAsync(h->d_sync, 0, sizeof(SyncWords), s);
     if (e == cudaSuccess) {
-      void* args[] = {&chunks,   &nc,       &max_norm,   &inv_scale, &wpartials, &h->d_result,
-                      &out_norm, &out_flag, &h->d_sync,  &expected,  &tmo};
+      SyncWords* sync = h->d_sync;
+      void* args[] = {&a, &sync, &tmo};
+      e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gclip::k_clip_persistent_tma),
+                                      dim3(h->grid_tma), dim3(gclip::kThreads), args, gclip::kTmaSmem,
+                                      s);
+    }
+    if (e == cudaSuccess && h->debug_extra > 0)
+      e = cudaMemsetAsync(h->d_sync, 0, sizeof(SyncWords), s);
+  } else {
+    mark(1);
+    mark(2);
+    gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag,
+                                  static_cast<unsigned int>(h->debug_extra));
+    long long tmo = h->timeout_ns;
+    if (e == cudaSuccess && h->debug_extra > 0)
+      e = cudaMemsetAsync(h->d_sync, 0, sizeof(SyncWords), s);
+    if (e == cudaSuccess) {
+      SyncWords* sync = h->d_sync;
+      void* args[] = {&a, &sync, &tmo};
       e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gclip::k_clip_persistent),
                                       dim3(h->grid_persistent), dim3(gclip::kThreads), args, 0, s);
     }
@@ -750,10 +1332,13 @@ extern "C" int clip_destroy(clip_handle_t h) {
 
 extern "C" int clip_set_variant(clip_handle_t h, int32_t variant) {
   if (h == nullptr) return GCLIP_ERR_INVALID_ARG;
-  if (variant != GCLIP_VARIANT_THREE_KERNEL && variant != GCLIP_VARIANT_PERSISTENT)
+  if (variant < GCLIP_VARIANT_SPLIT || variant > GCLIP_VARIANT_PERSISTENT_TMA)
     return GCLIP_ERR_INVALID_ARG;
-  if (variant == GCLIP_VARIANT_PERSISTENT && (!h->coop || (h->grid_persistent <= 0 && h->n_chunks > 0)))
-    return GCLIP_ERR_UNSUPPORTED;
+  const bool coop = variant == GCLIP_VARIANT_PERSISTENT || variant == GCLIP_VARIANT_PERSISTENT_TMA;
+  const int32_t grid = (variant == GCLIP_VARIANT_SPLIT_TMA || variant == GCLIP_VARIANT_PERSISTENT_TMA)
+                           ? h->grid_tma
+                           : h->grid_persistent;
+  if ((coop && !h->coop) || (grid <= 0 && h->n_chunks > 0)) return GCLIP_ERR_UNSUPPORTED;
   h->variant = variant;
   return GCLIP_OK;
 }
@@ -795,6 +1380,14 @@ extern "C" int clip_reset(clip_handle_t h, void* stream) {
 extern "C" int64_t clip_num_chunks(clip_handle_t h) { return h ? h->n_chunks : -1; }
 
 extern "C" int32_t clip_persistent_grid(clip_handle_t h) { return h ? h->grid_persistent : -1; }
+
+extern "C" int32_t clip_tma_grid(clip_handle_t h) { return h ? h->grid_tma : -1; }
+
+extern "C" int clip_set_l2_keep(clip_handle_t h, int64_t bytes) {
+  if (h == nullptr || bytes < 0) return GCLIP_ERR_INVALID_ARG;
+  set_keep(h, bytes);
+  return GCLIP_OK;
+}
 
 extern "C" int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals, int64_t timeout_ns) {
   if (h == nullptr || extra_arrivals < 0 || timeout_ns < 0) return GCLIP_ERR_INVALID_ARG;
@@ -840,7 +1433,7 @@ __global__ void __launch_bounds__(kThreads) k_grad_norm_partial_flat(uint64_t ba
   __shared__ FF red[kWarps];
   asm volatile("griddepcontrol.launch_dependents;");
   const clip_chunk_t c = flat_chunk(base, numel, dtype, blockIdx.x);
-  const FF acc = chunk_sumsq(c, inv_scale, red);
+  const FF acc = chunk_sumsq<PlainMem>(c, inv_scale, red, 0);
   if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
 }
 
@@ -853,7 +1446,7 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale_flat(uint64_t base, int
   if (!must_write(decision, chi, clo)) return;
   const clip_chunk_t c =
       flat_chunk(base, numel, dtype, n_chunks - 1 - static_cast<int64_t>(blockIdx.x));
-  chunk_scale(c, chi, clo);
+  chunk_scale<PlainMem>(c, chi, clo, 0);
 }
 
 }  // namespace gclip

@@ -59,12 +59,19 @@ extern "C" {
 #define GCLIP_DECISION_SKIP 2    /* nonfinite: no element was written      */
 
 /* ---- execution variants (clip_set_variant) ----------------------------- */
-#define GCLIP_VARIANT_THREE_KERNEL 0  /* partial sums, final reduce, scale:
-                                         three launches (the clipping page,
-                                         "ANDREA's three-kernel pipeline")  */
-#define GCLIP_VARIANT_PERSISTENT 1    /* the same three steps in one
-                                         cooperative launch with a
-                                         last-CTA-done reduction            */
+#define GCLIP_VARIANT_SPLIT 0       /* the clipping page's three steps
+                                       ("ANDREA's three-kernel pipeline")
+                                       in two launches: partial sums with
+                                       the final reduction done by the last
+                                       block to finish, then the scaling   */
+#define GCLIP_VARIANT_PERSISTENT 1  /* all three steps in one cooperative
+                                       launch: the last block to finish
+                                       reduces, the others wait for it on a
+                                       bounded grid barrier, then scale     */
+#define GCLIP_VARIANT_SPLIT_TMA 2   /* as SPLIT, with chunks staged through
+                                       shared memory by bulk (TMA) copies  */
+#define GCLIP_VARIANT_PERSISTENT_TMA 3  /* as PERSISTENT, staged by bulk
+                                       (TMA) copies                         */
 
 /* One gradient tensor: `numel` elements of format `dtype`, contiguous, in
  * device memory at `ptr` (aligned to the element size).  `reserved` must be
@@ -172,14 +179,15 @@ int clip_grad_norm(clip_handle_t h, float max_norm, float inv_scale,
 
 /* clip_grad_norm_profiled -- clip_grad_norm that also records four CUDA
  * events (cudaEvent_t handles created by the caller on the handle's device)
- * on `stream`: events[0] before the first launch, events[1] after the
- * partial sums, events[2] after the final reduction, events[3] after the
- * scaling pass.  With the single-launch variant the one launch lies between
- * events[0] and events[3], and events[1] and events[2] are recorded with
- * events[0].  Programmatic dependent launch is not used in this mode, so the
- * kernels do not overlap their neighbours; it is meant for measuring each
- * step of the clip, with the same arithmetic and results as clip_grad_norm.
- * Returns as clip_grad_norm, and GCLIP_ERR_INVALID_ARG for NULL events. */
+ * on `stream`: events[0] before the first launch, events[1] and events[2]
+ * after the norm pass (partial sums and final reduction, one launch),
+ * events[3] after the scaling pass.  With the single-launch variant the one
+ * launch lies between events[2] and events[3], and events[1] and events[2]
+ * are recorded with events[0].  Programmatic dependent launch is not used in
+ * this mode, so the launches do not overlap their neighbours; it is meant
+ * for measuring each step of the clip, with the same arithmetic and results
+ * as clip_grad_norm.  Returns as clip_grad_norm, and GCLIP_ERR_INVALID_ARG
+ * for NULL events. */
 int clip_grad_norm_profiled(clip_handle_t h, float max_norm, float inv_scale,
                             float *out_norm, int32_t *out_nonfinite_flag,
                             void *stream, void *const *events);
@@ -189,9 +197,11 @@ int clip_grad_norm_profiled(clip_handle_t h, float max_norm, float inv_scale,
  * GCLIP_ERR_CUDA if the device reported an error while finishing. */
 int clip_destroy(clip_handle_t h);
 
-/* clip_set_variant -- choose GCLIP_VARIANT_THREE_KERNEL or
- * GCLIP_VARIANT_PERSISTENT for later calls.  Both compute bit-identical
- * norms and outputs.  Returns GCLIP_ERR_INVALID_ARG for an unknown variant,
+/* clip_set_variant -- choose one of the GCLIP_VARIANT_* values for later
+ * calls (GCLIP_VARIANT_SPLIT is the default).  SPLIT and PERSISTENT compute
+ * bit-identical norms and outputs, and so do SPLIT_TMA and PERSISTENT_TMA;
+ * the two pairs sum in a different (fixed) order, so their norms can differ
+ * in the last bits.  Returns GCLIP_ERR_INVALID_ARG for an unknown variant,
  * GCLIP_ERR_UNSUPPORTED if the device cannot launch cooperative kernels. */
 int clip_set_variant(clip_handle_t h, int32_t variant);
 
@@ -221,6 +231,10 @@ int64_t clip_num_chunks(clip_handle_t h);
  * handle's device (-1 for NULL). */
 int32_t clip_persistent_grid(clip_handle_t h);
 
+/* clip_tma_grid -- thread blocks of the TMA variants on this handle's
+ * device (-1 for NULL). */
+int32_t clip_tma_grid(clip_handle_t h);
+
 /* clip_plan -- host-only: validate `descs` exactly as clip_create does and
  * write the chunk table it would build into `out` (capacity entries, may be
  * NULL to count).  Chunks follow tensor order; within a tensor they are
@@ -234,6 +248,14 @@ int clip_plan(const clip_tensor_desc_t *descs, int32_t n_tensors,
 
 /* clip_status_string -- a static English description of a return code. */
 const char *clip_status_string(int32_t code);
+
+/* clip_set_l2_keep -- how many bytes at the end of the norm pass (the
+ * chunks the scaling pass visits first) are read with an L2 evict_last
+ * policy, so that the scaling pass finds them in L2 instead of HBM.  The
+ * default is half the device's L2.  Rounded down to whole chunks; 0 turns
+ * the hint off.  Affects timing only, never results.  Returns GCLIP_OK or
+ * GCLIP_ERR_INVALID_ARG (NULL handle, negative bytes). */
+int clip_set_l2_keep(clip_handle_t h, int64_t bytes);
 
 /* clip_debug_barrier -- test hook for the single-launch variant's bounded
  * grid barrier.  extra_arrivals > 0 makes the barrier wait for that many

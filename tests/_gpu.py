@@ -20,7 +20,7 @@ NORM_RTOL = 1e-5
 ULP_TOL = {"f32": 2, "f16": 1, "bf16": 1}
 
 
-def gpu_clip(tensors, max_norm, inv_scale=1.0, variant="three_kernel", stream=None):
+def gpu_clip(tensors, max_norm, inv_scale=1.0, variant="split", stream=None):
     """Clip `tensors` (CUDA, in place) through the C ABI; return the record."""
     with g.GradClipper(tensors, variant=variant) as c:
         norm, flag = c.clip_(max_norm, inv_scale, stream=stream)

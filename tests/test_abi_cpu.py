@@ -174,6 +174,7 @@ def test_null_handle_calls(L):
     assert L.clip_read_result(None, None, None) == _abi.GCLIP_ERR_INVALID_ARG
     assert L.clip_reset(None, None) == _abi.GCLIP_ERR_INVALID_ARG
     assert L.clip_debug_barrier(None, 1, 0) == _abi.GCLIP_ERR_INVALID_ARG
+    assert L.clip_set_l2_keep(None, 0) == _abi.GCLIP_ERR_INVALID_ARG
 
 
 def test_status_strings(L):

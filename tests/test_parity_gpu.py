@@ -14,7 +14,7 @@ from workloads import WORKLOADS, make_gradset
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["three_kernel", "persistent"]
+VARIANTS = ["split", "persistent", "split_tma", "persistent_tma"]
 TD = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -79,10 +79,11 @@ def test_andrea120m(variant, name):
         assert res["worst_ulp"]["f16"] == 0
 
 
-def test_andrea1p2b():
+@pytest.mark.parametrize("variant", ["persistent", "split_tma"])
+def test_andrea1p2b(variant):
     gs = make_gradset("andrea1p2b", device=dev())
     before = host_copies(gs.tensors)
-    rec = gpu_clip(gs.tensors, gs.max_norm, gs.inv_scale, "persistent")
+    rec = gpu_clip(gs.tensors, gs.max_norm, gs.inv_scale, variant)
     res = compare(before, gs.tensors, rec, gs.max_norm, gs.inv_scale, "andrea1p2b")
     assert res["oracle"].decision == oracle.CLIP
 
@@ -242,13 +243,16 @@ def test_rejects_host_memory_descriptor():
 
 # -- determinism ----------------------------------------------------------------
 
-def test_bit_identical_runs_and_variants():
+@pytest.mark.parametrize("pair", [("split", "persistent"), ("split_tma", "persistent_tma")])
+def test_bit_identical_runs_and_variants(pair):
+    """20 runs alternating the two variants of one engine: the same norm,
+    sum of squares and multiplier bit for bit, and the same outputs."""
     gs = make_gradset("andrea120m", device=dev())
     pristine = clone_all(gs.tensors)
     records, outs = [], []
     with g.GradClipper(gs.tensors) as c:
         for i in range(20):
-            c.set_variant("three_kernel" if i % 2 == 0 else "persistent")
+            c.set_variant(pair[i % 2])
             restore(gs.tensors, pristine)
             c.clip_(gs.max_norm, gs.inv_scale)
             r = c.result()
@@ -276,10 +280,11 @@ def test_clip_twice_is_stable():
 
 # -- the single-launch variant's bounded barrier --------------------------------
 
-def test_barrier_timeout_reports_and_writes_nothing():
+@pytest.mark.parametrize("variant", ["persistent", "persistent_tma"])
+def test_barrier_timeout_reports_and_writes_nothing(variant):
     gs = make_gradset("andrea14m", device=dev())
     before = host_copies(gs.tensors)
-    with g.GradClipper(gs.tensors, variant="persistent") as c:
+    with g.GradClipper(gs.tensors, variant=variant) as c:
         c.debug_barrier(1, 20_000_000)     # one arrival that never comes; 20 ms
         c.clip_(1e-3)
         rec = c.result()
