@@ -46,7 +46,8 @@ constexpr long long kDefaultTimeoutNs = 1000000000LL;  // grid barrier: 1 s
 struct SyncWords {
   unsigned int arrive;  // blocks done with the norm pass in this call
   unsigned int gen;     // bumped once per call when the record is published
-  unsigned int pad[2];
+  unsigned int work;    // scaling-pass chunks claimed in this call
+  unsigned int pad;
 };
 
 // ---------------------------------------------------------------------------
@@ -570,10 +571,10 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-__global__ void __launch_bounds__(kThreads) k_clip_persistent(const NormArgs a, SyncWords* sync,
+__global__ void __launch_bounds__(kThreads, 5) k_clip_persistent(const NormArgs a, SyncWords* sync,
                                                               long long timeout_ns) {
   __shared__ FF red[kWarps];
-  __shared__ unsigned int s_gen0;
+  __shared__ unsigned int s_gen0, s_claim;
   __shared__ int s_flag, s_go;
 
   // The generation before this call.  It is bumped only after every block
@@ -586,13 +587,14 @@ __global__ void __launch_bounds__(kThreads) k_clip_persistent(const NormArgs a, 
 
   if (published) {
     if (threadIdx.x == 0) {
+      sync->work = 0u;  // nobody claims before the generation moves
+      __threadfence();
       atomicAdd(&sync->gen, 1u);  // release: the record was fenced above
       s_go = 1;
     }
   } else if (threadIdx.x == 0) {
     // Bounded wait for the record; on timeout flag it and write nothing.
     const unsigned long long t0 = globaltimer();
-    unsigned int ns = 32;
     int ok = 1;
     while (ld_acquire(&sync->gen) == s_gen0) {
       if (static_cast<long long>(globaltimer() - t0) > timeout_ns) {
@@ -600,8 +602,7 @@ __global__ void __launch_bounds__(kThreads) k_clip_persistent(const NormArgs a, 
         ok = 0;
         break;
       }
-      __nanosleep(ns);
-      if (ns < 1024) ns <<= 1;
+      __nanosleep(64);
     }
     __threadfence();
     s_go = ok;
@@ -612,11 +613,22 @@ __global__ void __launch_bounds__(kThreads) k_clip_persistent(const NormArgs a, 
   const int decision = __ldcg(&a.res->decision);
   const float chi = __ldcg(&a.res->coef_hi), clo = __ldcg(&a.res->coef_lo);
   if (!must_write(decision, chi, clo)) return;
-  // Phase 2: the same chunks in reverse order, most recently read first.
+  // Phase 2: chunks claimed one at a time from a shared counter, highest
+  // chunk first (most recently read).  Thread 0 claims the next chunk while
+  // the block scales the current one.
   const uint64_t pol = policy_evict_first();
-  for (int64_t k = blockIdx.x; k < a.n_chunks; k += gridDim.x) {
-    const clip_chunk_t ch = a.chunks[a.n_chunks - 1 - k];
-    chunk_scale<HintMem>(ch, chi, clo, pol);
+  const unsigned int n = static_cast<unsigned int>(a.n_chunks);
+  if (threadIdx.x == 0) s_claim = atomicAdd(&sync->work, 1u);
+  __syncthreads();
+  unsigned int claim = s_claim;
+  while (claim < n) {
+    unsigned int next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(&sync->work, 1u);
+    chunk_scale<HintMem>(a.chunks[n - 1u - claim], chi, clo, pol);
+    __syncthreads();
+    if (threadIdx.x == 0) s_claim = next;
+    __syncthreads();
+    claim = s_claim;
   }
 }
 
@@ -1191,7 +1203,7 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
     return GCLIP_ERR_CUDA;
   }
   h->l2_bytes = l2;
-  set_keep(h, static_cast<int64_t>(l2) / 2);
+  set_keep(h, 0);
   const int64_t resident = static_cast<int64_t>(sms) * per_sm;
   h->grid_persistent = static_cast<int32_t>(resident < h->n_chunks ? resident : h->n_chunks);
   const int64_t resident_tma = static_cast<int64_t>(sms) * per_sm_tma;
