@@ -52,6 +52,10 @@ def parse_args(argv=None):
     p.add_argument("--l2-keep-mb", type=float, default=None,
                    help="MB of the norm pass kept in L2 for the scaling pass "
                         "(default: the library's choice)")
+    p.add_argument("--warm", action="store_true",
+                   help="one set, no L2 flush (only for workloads that write nothing)")
+    p.add_argument("--graph", action="store_true",
+                   help="replay each run of clips as one captured CUDA graph")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -75,6 +79,20 @@ def rank_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def make_reduce_max(world: int, device):
+    """The max of a float over the ranks of the default process group (a
+    tensor on `device`: the GPU under NCCL, the CPU under gloo)."""
+    def reduce_max(x: float) -> float:
+        if world == 1:
+            return x
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return reduce_max
 
 
 def aggregate(elapsed_ms: float, units: float, world: int, reduce_max=None):
@@ -285,7 +303,7 @@ def run_gclip(args):
 
     # one pristine set, P working sets
     pristine = make_gradset(w, device=dev, flat=True)
-    P = max(1, min(args.pool, args.steps))
+    P = 1 if args.warm else max(1, min(args.pool, args.steps))
     sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
     clippers = [g.GradClipper(s.tensors, variant=args.variant) for s in sets]
     if args.l2_keep_mb is not None:
@@ -294,21 +312,32 @@ def run_gclip(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 + (1 << 20), dtype=torch.uint8, device=dev)
 
-    def restore():
-        for s in sets:
-            s.flat.copy_(pristine.flat)
-        flush.fill_(1)
+    writes = True
 
-    # correctness of the step being timed: the clip fires and the norm agrees
+    def restore():
+        # a clip that wrote changed its input: put the pristine values back
+        if writes:
+            for s in sets:
+                s.flat.copy_(pristine.flat)
+        if not args.warm:
+            flush.fill_(1)
+
+    # correctness of the step being timed: the decision and a norm that agrees
     # with a float64 torch norm of the same data (a sanity check, not parity)
     restore()
     clippers[0].clip_(w.max_norm, w.inv_scale)
     rec = clippers[0].result()
     ref_norm = math.sqrt(sum(float(t.double().square().sum()) for t in pristine.tensors)
                          ) * w.inv_scale
-    assert abs(rec["norm"] - ref_norm) <= 1e-5 * ref_norm, (rec["norm"], ref_norm)
+    if math.isfinite(ref_norm):
+        assert abs(rec["norm"] - ref_norm) <= 1e-5 * ref_norm, (rec["norm"], ref_norm)
+    else:
+        assert rec["nonfinite"] == 1, rec
     writes = rec["decision"] != g.GCLIP_DECISION_SKIP and not (
         rec["coef_hi"] == 1.0 and rec["coef_lo"] == 0.0)
+    if args.warm and writes:
+        print(json.dumps({"error": "--warm needs a workload whose clip writes nothing"}))
+        return 2
     decision_name = {0: "pass", 1: "clip", 2: "skip"}[rec["decision"]]
     nbytes = algorithmic_bytes(w.numel, w.elem_bytes, "write" if writes else "read")
 
@@ -329,12 +358,34 @@ def run_gclip(args):
     done = 0
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    graphs = {}
+
+    # clips per timed run: one per set of the pool; warm runs re-clip one set
+    run_len = args.pool if args.warm else P
+
+    def run_clips(n):
+        if not args.graph:
+            for i in range(n):
+                clippers[i % P].clip_(w.max_norm, w.inv_scale)
+            return
+        if n not in graphs:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for i in range(n):
+                    clippers[i % P].clip_(w.max_norm, w.inv_scale)
+            graphs[n] = gr
+            restore()
+            torch.cuda.synchronize()
+        graphs[n].replay()
+
     while done < args.steps:
-        n = min(P, args.steps - done)
+        n = min(run_len, args.steps - done)
         restore()
+        if args.graph and n not in graphs:
+            run_clips(n)          # capture (untimed), then restore again
+            restore()
         e0.record(stream)
-        for i in range(n):
-            clippers[i].clip_(w.max_norm, w.inv_scale)
+        run_clips(n)
         e1.record(stream)
         e1.synchronize()
         runs.append((e0.elapsed_time(e1), n))
@@ -346,12 +397,7 @@ def run_gclip(args):
 
     local_ms = sum(t for t, _ in runs)
 
-    def reduce_max(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    reduce_max = make_reduce_max(world, dev)
 
     value_bps, total_ms = aggregate(local_ms, nbytes * args.steps, world, reduce_max)
     per_step_ms = total_ms / args.steps
@@ -458,8 +504,10 @@ def run_gclip(args):
                 "workload": w.name, "description": w.description, "tensors": len(w.layout),
                 "elements": w.numel, "bytes_per_step": nbytes, "decision": decision_name,
                 "variant": args.variant, "pool": P, "l2_keep_mb": args.l2_keep_mb, "parallelism": f"replicas x{world}",
-                "l2": "inputs larger than L2 (one set per step, pool of distinct sets); "
-                      "L2 flushed before each timed run",
+                "l2": ("warm: one set re-read from L2, no flush" if args.warm else
+                       "inputs larger than L2 (one set per step, pool of distinct sets); "
+                       "L2 flushed before each timed run"),
+                "graph": bool(args.graph),
                 "timing": "CUDA events around each run of back-to-back clips on the "
                           "launching stream; restores between runs outside the events",
             },
