@@ -38,6 +38,16 @@ class _Tensor(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
+class _AdamwParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double),
+                ("step", ctypes.c_int64), ("zero_grads", ctypes.c_int32), ("pad", ctypes.c_int32)]
+
+
+class _AdamwState(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p)]
+
+
 class _Result(ctypes.Structure):
     _fields_ = [("sumsq", ctypes.c_double), ("norm", ctypes.c_double),
                 ("coef", ctypes.c_double), ("nonfinite", ctypes.c_int32),
@@ -111,6 +121,10 @@ class Oracle:
                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                          ctypes.POINTER(_Result)]
         L.oracle_clip_sample.restype = ctypes.c_int
+        L.oracle_clip_adamw.argtypes = [ctypes.POINTER(_Tensor), ctypes.POINTER(_AdamwState),
+                                        ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+                                        ctypes.POINTER(_AdamwParams), ctypes.POINTER(_Result)]
+        L.oracle_clip_adamw.restype = ctypes.c_int
         L.oracle_sumsq.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int32,
                                    ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_int32)]
@@ -164,6 +178,31 @@ class Oracle:
             raise ValueError("oracle_clip_sample rejected its arguments")
         return slots, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
                                    res.decision)
+
+    def clip_adamw(self, tensors, states, max_norm: float, inv_scale: float = 1.0, *,
+                   lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                   weight_decay: float = 0.0, step: int = 1, zero_grads: bool = False):
+        """Clip, then one AdamW step.  `states` is a list of (w, m, v) float32
+        arrays; returns (new gradients, [(w, m, v)], OracleResult); the inputs
+        are not modified."""
+        grads = [OracleTensor(t.data.copy(), t.dtype) for t in tensors]
+        new = [tuple(np.ascontiguousarray(a, dtype=np.float32).reshape(-1).copy() for a in st)
+               for st in states]
+        for t, (w, m, v) in zip(tensors, new):
+            if not (w.size == m.size == v.size == t.data.size):
+                raise ValueError("state arrays must match their gradient tensor")
+        sts = (_AdamwState * max(1, len(new)))()
+        for i, (w, m, v) in enumerate(new):
+            sts[i].w, sts[i].m, sts[i].v = (a.ctypes.data if a.size else None for a in (w, m, v))
+        p = _AdamwParams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                         int(step), int(bool(zero_grads)), 0)
+        res = _Result()
+        rc = self._lib.oracle_clip_adamw(self._descs(grads), sts, len(grads), float(max_norm),
+                                         float(inv_scale), ctypes.byref(p), ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_clip_adamw rejected its arguments")
+        return grads, new, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
+                                        res.decision)
 
     def clip_per_tensor(self, tensors, max_norm: float, inv_scale: float = 1.0):
         outs = [OracleTensor(t.data.copy(), t.dtype) for t in tensors]

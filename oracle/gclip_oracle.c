@@ -395,6 +395,110 @@ int oracle_clip_sample(const oracle_tensor *in, int32_t n_tensors,
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Clip, then one AdamW step on the clipped gradients.
+ *
+ * Order: "Grow a language model: gradient clipping" (unhomeschool.com),
+ * section "Order matters: Pre-Adam": the clip runs before the AdamW moments
+ * m, v and the weights are updated, so a spike never enters m and v.  Section
+ * "ANDREA-120M v1 ... Stability v2": v2 uses AdamW with clipping; section
+ * "Adjacent activities": AdamW keeps m and v.  "Grow a language model:
+ * backprop", section "Optimizer state": one m and one v per weight.
+ *
+ * The pages do not write the AdamW update out; the reading taken is the
+ * published algorithm with decoupled weight decay and bias correction:
+ *   g^ = x * inv_scale * coef             (the clipped, unscaled gradient)
+ *   m  = beta1 * m + (1 - beta1) * g^
+ *   v  = beta2 * v + (1 - beta2) * g^ * g^
+ *   w  = w - lr * wd * w - lr * (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ * w, m, v are fp32 arrays; every value is widened exactly to double and each
+ * result is rounded once to fp32.  On SKIP (a nonfinite gradient) nothing is
+ * updated and the gradients are not touched.  With zero_grads the gradients
+ * are set to +0 after use (the backprop page, "Accumulation across
+ * microbatches": zero_grads() resets the buffers after the optimizer step). */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;      /* 1-based */
+    int32_t zero_grads;
+    int32_t pad;
+} oracle_adamw_params;
+
+typedef struct {
+    void *w, *m, *v;   /* fp32, numel of the matching gradient tensor */
+} oracle_adamw_state;
+
+static float ld_f32(const void *p, int64_t i)
+{
+    float x;
+    memcpy(&x, (const char *)p + 4 * i, 4);
+    return x;
+}
+
+static void st_f32(void *p, int64_t i, double v)
+{
+    float x = (float)v;
+    memcpy((char *)p + 4 * i, &x, 4);
+}
+
+int oracle_clip_adamw(const oracle_tensor *g, const oracle_adamw_state *st,
+                      int32_t n_tensors, double max_norm, double inv_scale,
+                      const oracle_adamw_params *p, oracle_result *res)
+{
+    if (p->step < 1 || !(p->lr >= 0.0) || !(p->eps > 0.0) ||
+        !(p->beta1 >= 0.0 && p->beta1 < 1.0) ||
+        !(p->beta2 >= 0.0 && p->beta2 < 1.0))
+        return -1;
+    if (decide(g, n_tensors, max_norm, inv_scale, res) != 0)
+        return -1;
+    if (res->decision == OR_DECISION_SKIP)
+        return 0;
+    double bc1 = 1.0 - pow(p->beta1, (double)p->step);
+    double bc2 = 1.0 - pow(p->beta2, (double)p->step);
+    for (int32_t t = 0; t < n_tensors; ++t) {
+        for (int64_t i = 0; i < g[t].numel; ++i) {
+            double x = oracle_decode(g[t].data, i, g[t].dtype);
+#if ORACLE_MUTANT == 14
+            double gh = x * inv_scale;         /* mistake: Adam sees the raw gradient */
+#else
+            double gh = clipped_value(x, inv_scale, res->coef);
+#endif
+            double w = ld_f32(st[t].w, i);
+            double m = ld_f32(st[t].m, i);
+            double v = ld_f32(st[t].v, i);
+#if ORACLE_MUTANT == 13
+            gh += p->weight_decay * w;         /* mistake: L2 decay, not decoupled */
+#endif
+            m = p->beta1 * m + (1.0 - p->beta1) * gh;
+#if ORACLE_MUTANT == 15
+            v = p->beta1 * v + (1.0 - p->beta1) * gh * gh;  /* mistake: beta1 in v */
+#else
+            v = p->beta2 * v + (1.0 - p->beta2) * gh * gh;
+#endif
+#if ORACLE_MUTANT == 11
+            double mh = m, vh = v;             /* mistake: no bias correction */
+#else
+            double mh = m / bc1, vh = v / bc2;
+#endif
+#if ORACLE_MUTANT == 12
+            double upd = mh / sqrt(vh + p->eps);   /* mistake: eps inside sqrt */
+#else
+            double upd = mh / (sqrt(vh) + p->eps);
+#endif
+#if ORACLE_MUTANT == 13
+            w = w - p->lr * upd;
+#else
+            w = w - p->lr * p->weight_decay * w - p->lr * upd;
+#endif
+            st_f32(st[t].w, i, w);
+            st_f32(st[t].m, i, m);
+            st_f32(st[t].v, i, v);
+            if (p->zero_grads)
+                oracle_encode((void *)g[t].data, i, g[t].dtype, 0.0);
+        }
+    }
+    return 0;
+}
+
 /* Per-coordinate (value) clipping to [-c, c], the contrast drawn on the
  * glossary page, section "Shorten the arrow, keep the direction": each
  * element is clamped on its own, which can change the direction.  Used only

@@ -366,4 +366,101 @@ def pin_sampled_outputs_match_full_clip(o):
         assert np.array_equal(got, want)
 
 
+# -- clip, then AdamW (the clipping page, "Order matters: Pre-Adam") ----------
+
+def _adamw_case(seed, sizes=(37, 5), dt="f32", scale=1e-3):
+    rng = np.random.default_rng(seed)
+    grads = [make(rng.normal(0, scale, n), dt) for n in sizes]
+    states = [(rng.normal(0, 0.02, n).astype(np.float32),
+               rng.normal(0, 1e-4, n).astype(np.float32),
+               np.abs(rng.normal(0, 1e-8, n)).astype(np.float32)) for n in sizes]
+    return grads, states
+
+
+def pin_adamw_matches_torch(o):
+    """The AdamW step of the oracle equals torch.optim.AdamW (float64, one
+    step, the same clipped gradient and state) after rounding to fp32."""
+    for step, wd, dt in ((1, 0.0, "f32"), (1, 0.1, "f16"), (7, 0.1, "f32"), (200, 0.01, "bf16")):
+        grads, states = _adamw_case(step, dt=dt)
+        c, s_inv = 1e-3, 0.5                    # norm ~3e-3: the clip fires
+        hp = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=wd, step=step)
+        _, new, r = o.clip_adamw(grads, states, c, s_inv, **hp)
+        assert r.decision == CLIP
+        for gt, (w, m, v), (w1, m1, v1) in zip(grads, states, new):
+            param = torch.tensor(w, dtype=torch.float64, requires_grad=True)
+            opt = torch.optim.AdamW([param], lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]),
+                                    eps=hp["eps"], weight_decay=wd, foreach=False)
+            opt.state[param] = {"step": torch.tensor(float(step - 1)),
+                                "exp_avg": torch.tensor(m, dtype=torch.float64),
+                                "exp_avg_sq": torch.tensor(v, dtype=torch.float64)}
+            param.grad = torch.tensor(as_float64(gt) * s_inv * r.coef, dtype=torch.float64)
+            opt.step()
+            st = opt.state[param]
+            for ours, theirs in ((w1, param.detach()), (m1, st["exp_avg"]), (v1, st["exp_avg_sq"])):
+                ref = theirs.numpy().astype(np.float32)
+                d = np.abs(ours.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+                assert d.max() <= 1, (step, dt, d.max())
+
+
+def pin_adamw_first_step_closed_form(o):
+    """From m = v = 0 at step 1 the bias-corrected moments are g^ and g^^2,
+    so w' = w (1 - lr wd) - lr g^ / (|g^| + eps)."""
+    x = np.array([3e-3, -4e-3, 1e-6, 0.0], np.float32)
+    w = np.array([0.5, -0.25, 1e-3, 2.0], np.float32)
+    z = np.zeros(4, np.float32)
+    lr, wd, eps = 1e-3, 0.05, 1e-8
+    _, new, r = o.clip_adamw([make(x, "f32")], [(w, z, z)], 1.0, 1.0, lr=lr, beta1=0.9,
+                             beta2=0.999, eps=eps, weight_decay=wd, step=1)
+    assert r.decision == PASS
+    gh = x.astype(np.float64)
+    want = w.astype(np.float64) * (1 - lr * wd) - lr * gh / (np.abs(gh) + eps)
+    assert np.array_equal(new[0][0], want.astype(np.float32))
+    assert np.array_equal(new[0][1], (0.1 * gh).astype(np.float32))
+    assert np.array_equal(new[0][2], (0.001 * gh * gh).astype(np.float32))
+
+
+def pin_adamw_update_bound(o):
+    """The clipping page, "Adjacent activities": with warm-up lr 1.5e-7 and
+    max_norm 1 the worst-case first-step change of a parameter is
+    lr x max_norm = 1.5e-7, even under a 50x spike."""
+    rng = np.random.default_rng(21)
+    x = rng.normal(0, 3e-5, 5000)
+    x[100:600] *= 50.0
+    w = rng.normal(0, 1e-4, 5000).astype(np.float32)
+    z = np.zeros(5000, np.float32)
+    _, new, r = o.clip_adamw([make(x, "f32")], [(w, z, z)], 1.0, 1.0, lr=1.5e-7, step=1)
+    dw = np.abs(new[0][0].astype(np.float64) - w.astype(np.float64))
+    # plus the rounding of the stored fp32 weight
+    assert np.all(dw <= 1.5e-7 + np.spacing(np.abs(new[0][0])).astype(np.float64)), dw.max()
+
+
+def pin_adamw_pre_adam(o):
+    """Pre-Adam order: the first moment sees the clipped gradient, so a spike
+    enters m at max_norm / norm of its size."""
+    x = np.array([600.0, 800.0], np.float32)        # norm 1000
+    z = np.zeros(2, np.float32)
+    _, new, r = o.clip_adamw([make(x, "f32")], [(z, z, z)], 1.0, 1.0, lr=1e-3, beta1=0.9,
+                             step=1)
+    assert r.decision == CLIP and r.coef == 1e-3
+    assert np.array_equal(new[0][1], np.array([0.06, 0.08], np.float32))   # 0.1 * [0.6, 0.8]
+
+
+def pin_adamw_skip_and_zero_grads(o):
+    """A nonfinite gradient stops the update: w, m, v and the gradients stay
+    as they were.  Otherwise zero_grads leaves every gradient at +0."""
+    grads, states = _adamw_case(3)
+    bad = [grads[0], make([1.0, math.nan], "f32")]
+    sts = [states[0], (np.ones(2, np.float32),) * 3]
+    g2, new, r = o.clip_adamw(bad, sts, 1.0, lr=1e-3, zero_grads=True)
+    assert r.decision == SKIP
+    for (a, b), (c, d) in zip(zip(sts, new), zip(bad, g2)):
+        for x, y in zip(a, b):
+            assert np.array_equal(x.view(np.int32), y.view(np.int32))
+        assert np.array_equal(storage_bits(c), storage_bits(d))
+    g3, _, r = o.clip_adamw(grads, states, 1e-6, lr=1e-3, zero_grads=True)
+    assert r.decision == CLIP
+    for t in g3:
+        assert not storage_bits(t).any()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

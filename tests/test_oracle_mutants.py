@@ -21,6 +21,11 @@ MUTANTS = {
     8: "square root missing",
     9: "outputs not unscaled",
     10: "sign of the output flipped",
+    11: "AdamW without bias correction",
+    12: "AdamW eps inside the square root",
+    13: "AdamW weight decay coupled into the gradient",
+    14: "AdamW fed the unclipped gradient",
+    15: "AdamW second moment with beta1",
 }
 
 
