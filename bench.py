@@ -56,6 +56,8 @@ def parse_args(argv=None):
                    help="one set, no L2 flush (only for workloads that write nothing)")
     p.add_argument("--graph", action="store_true",
                    help="replay each run of clips as one captured CUDA graph")
+    p.add_argument("--adamw", action="store_true",
+                   help="time the fused clip + AdamW step instead of the clip alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -530,10 +532,128 @@ def run_gclip(args):
     return 0
 
 
+def run_adamw(args):
+    """The fused clip + AdamW step (clip_grad_norm_adamw) on the ANDREA set,
+    beside the unfused pipeline: this library's clip, then torch's fused
+    AdamW on the same tensors.  One JSON line."""
+    import torch
+
+    import global_l2_norm_gb300 as g
+    from workloads import WORKLOADS, make_gradset
+
+    dev = torch.device("cuda", 0)
+    g.build()
+    w = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(dev)
+    P = max(1, min(args.pool, args.steps))
+    pristine = make_gradset(w, device=dev, flat=True)
+    sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
+    states = []
+    for s in sets:
+        st = [tuple(torch.zeros(t.numel(), device=dev) for _ in range(3)) for t in s.tensors]
+        for (wt, _, _) in st:
+            wt.normal_(0.0, 0.02)
+        states.append(st)
+    clippers = [g.GradClipper(s.tensors) for s in sets]
+    for c, st in zip(clippers, states):
+        c.attach_adamw(st)
+    hp = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 + (1 << 20), dtype=torch.uint8, device=dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, steps, restore):
+        total, done = 0.0, 0
+        while done < steps:
+            n = min(P, steps - done)
+            restore()
+            flush.fill_(1)
+            e0.record(stream)
+            for i in range(n):
+                fn(i)
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+            done += n
+        return total / steps
+
+    step_no = [0]
+
+    def fused(i):
+        step_no[0] += 1
+        clippers[i].clip_adamw_(w.max_norm, w.inv_scale, step=step_no[0], **hp)
+
+    # correctness of what is timed: the clip fires on this workload
+    clippers[0].clip_adamw_(w.max_norm, w.inv_scale, step=1, **hp)
+    decision = clippers[0].result()["decision"]
+    timed(fused, args.warmup, lambda: None)
+    fused_ms = timed(fused, args.steps, lambda: None)
+
+    # unfused: clip (rewrites the gradients), then torch's fused AdamW
+    params = [[torch.nn.Parameter(st[0].view(t.shape)) for st, t in zip(states[i], sets[i].tensors)]
+              for i in range(P)]
+    for i in range(P):
+        for prm, t in zip(params[i], sets[i].tensors):
+            prm.grad = t if t.dtype == torch.float32 else None
+    have_torch = all(p_.grad is not None for ps in params for p_ in ps)
+    unfused_ms = None
+    if have_torch:
+        opts = [torch.optim.AdamW(ps, fused=True, **{k: v for k, v in hp.items()
+                                                     if k not in ("beta1", "beta2")},
+                                  betas=(hp["beta1"], hp["beta2"])) for ps in params]
+
+        def unfused(i):
+            clippers[i].clip_(w.max_norm, w.inv_scale)
+            opts[i].step()
+
+        def restore_grads():
+            for s in sets:
+                s.flat.copy_(pristine.flat)
+
+        timed(unfused, args.warmup, restore_grads)
+        unfused_ms = timed(unfused, args.steps, restore_grads)
+
+    es = w.elem_bytes
+    fused_bytes = w.numel * (2 * es + 24)        # g read twice; w, m, v read and written
+    # clip 3 * es; AdamW reads g, w, m, v and writes w, m, v
+    unfused_bytes = w.numel * (3 * es + 4 + 12 + 12) if have_torch else None
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs") or 6800.0
+    value = fused_bytes / (fused_ms / 1e3) / 1e9
+    line = {
+        "metric": "fused clip + AdamW step GB/s (algorithmic), " + w.name,
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(fused_ms, 5), "higher_is_better": True,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "decision": {0: "pass", 1: "clip", 2: "skip"}[decision],
+                   "bytes_per_step": fused_bytes, "pool": P, "adamw": hp,
+                   "l2": "pool of distinct sets, L2 flushed before each timed run"},
+        "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4)},
+        "unfused": None if unfused_ms is None else {
+            "what": "clip_grad_norm (split) then torch.optim.AdamW(fused=True); the time "
+                    "includes torch's host-side optimizer overhead",
+            "ms_per_step": round(unfused_ms, 5), "bytes_per_step": unfused_bytes,
+            "speedup_of_fused": round(unfused_ms / fused_ms, 3)},
+    }
+    for c in clippers:
+        c.close()
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.adamw:
+        return run_adamw(args)
     return run_gclip(args)
 
 

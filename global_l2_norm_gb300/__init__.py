@@ -116,6 +116,33 @@ class GradClipper:
             out_flag.data_ptr(), _stream_handle(stream, self.device)))
         return out_norm, out_flag
 
+    # -- fused clip + AdamW --------------------------------------------------
+    def attach_adamw(self, states) -> None:
+        """Attach fp32 (w, m, v) CUDA tensors, one triple per gradient tensor
+        (same numel), for clip_adamw_.  They stay owned by the caller."""
+        states = list(states)
+        arr = (_abi.clip_adamw_state_t * max(1, len(states)))()
+        for i, (w, m, v) in enumerate(states):
+            for a in (w, m, v):
+                if a.dtype != torch.float32 or not a.is_contiguous() or a.device != self.device:
+                    raise ValueError("AdamW state must be contiguous fp32 on the gradients' device")
+            arr[i].w, arr[i].m, arr[i].v = (a.data_ptr() if a.numel() else None for a in (w, m, v))
+        self._states = states
+        check("clip_attach_adamw", self._lib.clip_attach_adamw(self._h, arr, len(states)))
+
+    def clip_adamw_(self, max_norm: float, inv_scale: float = 1.0, *, lr: float,
+                    beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                    weight_decay: float = 0.0, step: int = 1, zero_grads: bool = False,
+                    stream=None):
+        """Clip, then one AdamW step on the attached state (see
+        clip_grad_norm_adamw in include/gclip.h).  Returns (norm, flag)."""
+        p = _abi.clip_adamw_params_t(float(lr), float(beta1), float(beta2), float(eps),
+                                     float(weight_decay), int(bool(zero_grads)))
+        check("clip_grad_norm_adamw", self._lib.clip_grad_norm_adamw(
+            self._h, float(max_norm), float(inv_scale), ctypes.byref(p), int(step),
+            self.norm.data_ptr(), self.flag.data_ptr(), _stream_handle(stream, self.device)))
+        return self.norm, self.flag
+
     # -- configuration and inspection -----------------------------------
     def set_variant(self, variant) -> None:
         v = VARIANTS[variant] if isinstance(variant, str) else int(variant)

@@ -53,6 +53,16 @@ class clip_result_t(ctypes.Structure):
                 ("calls", ctypes.c_uint32), ("reserved", ctypes.c_int32)]
 
 
+class clip_adamw_state_t(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p)]
+
+
+class clip_adamw_params_t(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("zero_grads", ctypes.c_int32)]
+
+
 class clip_chunk_t(ctypes.Structure):
     _fields_ = [("addr", ctypes.c_uint64), ("numel", ctypes.c_uint32),
                 ("meta", ctypes.c_uint32)]
@@ -80,6 +90,10 @@ _SIGNATURES = {
     "clip_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "clip_debug_barrier": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
     "clip_set_l2_keep": (ctypes.c_int, [_P, ctypes.c_int64]),
+    "clip_attach_adamw": (ctypes.c_int, [_P, ctypes.POINTER(clip_adamw_state_t), ctypes.c_int32]),
+    "clip_grad_norm_adamw": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float,
+                                            ctypes.POINTER(clip_adamw_params_t), ctypes.c_int64,
+                                            _P, _P, _P]),
     "clip_grad_norm_flat_noalloc": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_float, _P, _P, _P]),
 }

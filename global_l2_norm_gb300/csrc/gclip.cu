@@ -557,6 +557,127 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __r
 }
 
 // ---------------------------------------------------------------------------
+// Fused clip + AdamW: after the norm pass, one pass over gradients and state
+// that forms the clipped gradient in registers and updates w, m, v.
+
+struct TensorState {
+  uint64_t g, w, m, v;  // gradient base and the fp32 state arrays of one tensor
+};
+
+struct AdamwArgs {
+  float beta1, beta2, omb1, omb2;  // beta and 1 - beta, each rounded once to fp32
+  float inv_bc1, inv_bc2;          // 1 / (1 - beta^step), from double
+  float eps, lr, decay;            // decay = 1 - lr * weight_decay, from double
+  int zero_grads;
+};
+
+// One element: g^ = x * (chi + clo) rounded once, then the moments and the
+// weight, each with IEEE-rounded fp32 operations.
+__device__ __forceinline__ void adamw1(float x, float& w, float& m, float& v, float chi, float clo,
+                                       const AdamwArgs& p) {
+  const float gh = __fmaf_rn(x, chi, __fmul_rn(x, clo));
+  m = __fmaf_rn(p.beta1, m, __fmul_rn(p.omb1, gh));
+  v = __fmaf_rn(p.beta2, v, __fmul_rn(p.omb2, __fmul_rn(gh, gh)));
+  const float denom = __fadd_rn(__fsqrt_rn(__fmul_rn(v, p.inv_bc2)), p.eps);
+  const float upd = __fdiv_rn(__fmul_rn(m, p.inv_bc1), denom);
+  w = __fmaf_rn(-p.lr, upd, __fmul_rn(w, p.decay));
+}
+
+__device__ __forceinline__ void adamw4(const float (&x)[4], float4* w, float4* m, float4* v, float chi,
+                                       float clo, const AdamwArgs& p) {
+  float4 W = __ldcs(w), M = __ldcs(m), V = __ldcs(v);
+  adamw1(x[0], W.x, M.x, V.x, chi, clo, p);
+  adamw1(x[1], W.y, M.y, V.y, chi, clo, p);
+  adamw1(x[2], W.z, M.z, V.z, chi, clo, p);
+  adamw1(x[3], W.w, M.w, V.w, chi, clo, p);
+  __stcs(w, W);
+  __stcs(m, M);
+  __stcs(v, V);
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_vec(uint4 g, float (&x)[8]) {
+  if constexpr (DT == GCLIP_F32) {
+    x[0] = __uint_as_float(g.x);
+    x[1] = __uint_as_float(g.y);
+    x[2] = __uint_as_float(g.z);
+    x[3] = __uint_as_float(g.w);
+  } else {
+    const float2 a = Fmt<DT>::widen(g.x), b = Fmt<DT>::widen(g.y), c = Fmt<DT>::widen(g.z),
+                 d = Fmt<DT>::widen(g.w);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void adamw_chunk(const clip_chunk_t& c, const TensorState& ts, float chi,
+                                            float clo, const AdamwArgs& p) {
+  constexpr uint32_t E = Fmt<DT>::kPerVec, B = Fmt<DT>::kBytes;
+  const Span sp = make_span<DT>(c.addr, c.numel);
+  const uint64_t e0 = (c.addr - ts.g) / B;  // index of the chunk's first element
+  float* w = reinterpret_cast<float*>(ts.w) + e0;
+  float* m = reinterpret_cast<float*>(ts.m) + e0;
+  float* v = reinterpret_cast<float*>(ts.v) + e0;
+  const uint64_t pol = policy_evict_first();
+  uint4* gv = reinterpret_cast<uint4*>(sp.body);
+  const bool vec = ((reinterpret_cast<uint64_t>(w + sp.head) | reinterpret_cast<uint64_t>(m + sp.head) |
+                     reinterpret_cast<uint64_t>(v + sp.head)) & 15u) == 0;
+  if (vec) {
+    for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) {
+      float x[8];
+      widen_vec<DT>(HintMem::ld_scale(gv + i, pol), x);
+      const uint32_t k = sp.head + i * E;
+#pragma unroll
+      for (uint32_t q = 0; q < E; q += 4) {
+        const float xs[4] = {x[q], x[q + 1], x[q + 2], x[q + 3]};
+        adamw4(xs, reinterpret_cast<float4*>(w + k + q), reinterpret_cast<float4*>(m + k + q),
+               reinterpret_cast<float4*>(v + k + q), chi, clo, p);
+      }
+      if (p.zero_grads) HintMem::st_scale(gv + i, make_uint4(0, 0, 0, 0), pol);
+    }
+  } else {
+    // state not 16-byte aligned with the gradient: element by element
+    for (uint32_t j = sp.head + threadIdx.x; j < sp.tail_start; j += kThreads) {
+      const uint64_t a = c.addr + static_cast<uint64_t>(j) * B;
+      float W = w[j], M = m[j], V = v[j];
+      adamw1(Fmt<DT>::load1(a), W, M, V, chi, clo, p);
+      w[j] = W;
+      m[j] = M;
+      v[j] = V;
+      if (p.zero_grads) Fmt<DT>::store1(a, 0.0f);
+    }
+  }
+  for (uint32_t j = threadIdx.x; j < sp.head + sp.ntail; j += kThreads) {
+    const uint32_t k = j < sp.head ? j : sp.tail_start + (j - sp.head);
+    const uint64_t a = c.addr + static_cast<uint64_t>(k) * B;
+    float W = w[k], M = m[k], V = v[k];
+    adamw1(Fmt<DT>::load1(a), W, M, V, chi, clo, p);
+    w[k] = W;
+    m[k] = M;
+    v[k] = V;
+    if (p.zero_grads) Fmt<DT>::store1(a, 0.0f);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_adamw(const clip_chunk_t* __restrict__ chunks,
+                                                    int64_t n_chunks,
+                                                    const TensorState* __restrict__ states,
+                                                    const clip_result_t* res, const AdamwArgs p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (__ldcg(&res->decision) == GCLIP_DECISION_SKIP) return;
+  const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
+  // Highest chunks first: the norm pass read their gradients last.
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const TensorState ts = states[c.meta >> 8];
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: adamw_chunk<GCLIP_F32>(c, ts, chi, clo, p); break;
+    case GCLIP_F16: adamw_chunk<GCLIP_F16>(c, ts, chi, clo, p); break;
+    default: adamw_chunk<GCLIP_BF16>(c, ts, chi, clo, p); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Single-launch variant (cooperative launch, so every block is resident).
 
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
@@ -1073,6 +1194,8 @@ struct gclip_handle {
   float2* d_partials;        // one entry per block of the norm pass (G)
   clip_result_t* d_result;
   SyncWords* d_sync;
+  std::vector<clip_tensor_desc_t> descs;   // the gradient tensors, as created
+  gclip::TensorState* d_states;            // AdamW state table (NULL until attached)
 };
 
 namespace {
@@ -1153,6 +1276,7 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   }
   h->n_chunks = static_cast<int64_t>(chunks.size());
   h->variant = GCLIP_VARIANT_SPLIT;
+  h->descs.assign(descs, descs + n_tensors);
   h->timeout_ns = gclip::kDefaultTimeoutNs;
 
   const size_t n = chunks.size();
@@ -1336,6 +1460,7 @@ extern "C" int clip_destroy(clip_handle_t h) {
     DeviceGuard guard(h->device);
     if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) rc = GCLIP_ERR_CUDA;
     if (cudaFree(h->arena) != cudaSuccess) rc = GCLIP_ERR_CUDA;
+    if (h->d_states != nullptr && cudaFree(h->d_states) != cudaSuccess) rc = GCLIP_ERR_CUDA;
     cudaGetLastError();
   }
   delete h;
@@ -1405,6 +1530,105 @@ extern "C" int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals, int64
   if (h == nullptr || extra_arrivals < 0 || timeout_ns < 0) return GCLIP_ERR_INVALID_ARG;
   h->debug_extra = extra_arrivals;
   h->timeout_ns = timeout_ns > 0 ? timeout_ns : gclip::kDefaultTimeoutNs;
+  return GCLIP_OK;
+}
+
+extern "C" int clip_attach_adamw(clip_handle_t h, const clip_adamw_state_t* states,
+                                 int32_t n_tensors) {
+  if (h == nullptr || n_tensors != static_cast<int32_t>(h->descs.size()) ||
+      (n_tensors > 0 && states == nullptr))
+    return GCLIP_ERR_INVALID_ARG;
+  std::vector<clip_tensor_desc_t> all(h->descs);  // gradients, then w, m, v of each tensor
+  std::vector<gclip::TensorState> table(static_cast<size_t>(n_tensors));
+  for (int32_t t = 0; t < n_tensors; ++t) {
+    const clip_tensor_desc_t& d = h->descs[t];
+    table[t].g = reinterpret_cast<uint64_t>(d.ptr);
+    table[t].w = reinterpret_cast<uint64_t>(states[t].w);
+    table[t].m = reinterpret_cast<uint64_t>(states[t].m);
+    table[t].v = reinterpret_cast<uint64_t>(states[t].v);
+    if (d.numel == 0) continue;
+    for (float* a : {states[t].w, states[t].m, states[t].v}) {
+      clip_tensor_desc_t s = {a, d.numel, GCLIP_F32, 0};
+      all.push_back(s);
+    }
+  }
+  if (gclip::validate_descs(all.data(), static_cast<int32_t>(all.size())) != GCLIP_OK)
+    return GCLIP_ERR_INVALID_ARG;  // NULL, misaligned or overlapping
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  gclip::TensorState* d = nullptr;
+  const size_t bytes = sizeof(gclip::TensorState) * (table.empty() ? 1 : table.size());
+  cudaError_t e = cudaMalloc(&d, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? GCLIP_ERR_OOM : GCLIP_ERR_CUDA;
+  }
+  if (!table.empty())
+    e = cudaMemcpy(d, table.data(), table.size() * sizeof(gclip::TensorState),
+                   cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(d);
+    return GCLIP_ERR_CUDA;
+  }
+  if (h->d_states != nullptr) {
+    cudaDeviceSynchronize();  // the old table may still be read by queued work
+    cudaFree(h->d_states);
+  }
+  h->d_states = d;
+  return GCLIP_OK;
+}
+
+extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
+                                    const clip_adamw_params_t* p, int64_t step, float* out_norm,
+                                    int32_t* out_nonfinite_flag, void* stream) {
+  if (h == nullptr || p == nullptr || h->d_states == nullptr || !valid_scalar(max_norm) ||
+      !valid_scalar(inv_scale) || step < 1)
+    return GCLIP_ERR_INVALID_ARG;
+  const bool ok = std::isfinite(p->lr) && p->lr >= 0.0f && std::isfinite(p->eps) && p->eps > 0.0f &&
+                  std::isfinite(p->weight_decay) && p->weight_decay >= 0.0f && p->beta1 >= 0.0f &&
+                  p->beta1 < 1.0f && p->beta2 >= 0.0f && p->beta2 < 1.0f;
+  if (!ok) return GCLIP_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t nc = h->n_chunks;
+  cudaError_t e = cudaSuccess;
+  if (nc == 0) {
+    const float2* partials = h->d_partials;
+    void* args[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm,
+                    &out_nonfinite_flag};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, args, false);
+  } else {
+    gclip::NormArgs a =
+        norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_nonfinite_flag, 0);
+    void* a1[] = {&a};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial),
+                   static_cast<unsigned int>(h->grid_persistent), s, a1, false);
+    gclip::AdamwArgs q;
+    const double b1 = p->beta1, b2 = p->beta2;
+    q.beta1 = p->beta1;
+    q.beta2 = p->beta2;
+    q.omb1 = static_cast<float>(1.0 - b1);
+    q.omb2 = static_cast<float>(1.0 - b2);
+    q.inv_bc1 = static_cast<float>(1.0 / (1.0 - std::pow(b1, static_cast<double>(step))));
+    q.inv_bc2 = static_cast<float>(1.0 / (1.0 - std::pow(b2, static_cast<double>(step))));
+    q.eps = p->eps;
+    q.lr = p->lr;
+    q.decay = static_cast<float>(1.0 - static_cast<double>(p->lr) * p->weight_decay);
+    q.zero_grads = p->zero_grads ? 1 : 0;
+    const clip_chunk_t* chunks = h->d_chunks;
+    const gclip::TensorState* st = h->d_states;
+    const clip_result_t* cres = h->d_result;
+    void* a2[] = {&chunks, &nc, &st, &cres, &q};
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_adamw), static_cast<unsigned int>(nc), s,
+                     a2, true);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
   return GCLIP_OK;
 }
 

@@ -268,6 +268,67 @@ int clip_set_l2_keep(clip_handle_t h, int64_t bytes);
 int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals,
                        int64_t timeout_ns);
 
+/* ---- fused clip + AdamW ---------------------------------------------------
+ *
+ * Source: the clipping page, section "Order matters: Pre-Adam": the clip runs
+ * before the AdamW moments m, v and the weights are updated, so a spike never
+ * reaches m and v; section "Adjacent activities": AdamW keeps m and v.  The
+ * backprop page, section "Optimizer state": one m and one v per weight, and
+ * section "Accumulation across microbatches": zero_grads() after the step.
+ * The pages do not write the update out; it is the published AdamW with
+ * decoupled weight decay and bias correction, on g^ = x * multiplier (the
+ * clipped, unscaled gradient of clip_grad_norm):
+ *   m = beta1 m + (1 - beta1) g^;  v = beta2 v + (1 - beta2) g^^2
+ *   w = w (1 - lr wd) - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ * Fusing it makes the clip's scaling pass unnecessary: the clipped gradient
+ * is formed in registers, never stored. */
+
+/* The optimizer state of one gradient tensor: fp32 device arrays with the
+ * tensor's numel, each aligned to 4 bytes (16 bytes, like the gradient,
+ * lets the kernel use vector access).  Owned by the caller. */
+typedef struct {
+    float *w;
+    float *m;
+    float *v;
+} clip_adamw_state_t;
+
+typedef struct {
+    float lr;            /* >= 0 */
+    float beta1;         /* in [0, 1) */
+    float beta2;         /* in [0, 1) */
+    float eps;           /* > 0 */
+    float weight_decay;  /* >= 0, decoupled */
+    int32_t zero_grads;  /* nonzero: write +0 to every gradient element after
+                            use (not on SKIP) */
+} clip_adamw_params_t;
+
+/* clip_attach_adamw -- give the handle the optimizer state of its tensors,
+ * states[i] for descriptor i (n_tensors must equal the handle's count;
+ * empty tensors may have NULL pointers).  Checks alignment and that no two
+ * arrays (weights, moments, gradients) overlap; copies a table of pointers to
+ * the device (the only allocation, at attach time).  May be called again to
+ * replace the state.  Returns GCLIP_OK, GCLIP_ERR_INVALID_ARG, GCLIP_ERR_OOM
+ * or GCLIP_ERR_CUDA. */
+int clip_attach_adamw(clip_handle_t h, const clip_adamw_state_t *states,
+                      int32_t n_tensors);
+
+/* clip_grad_norm_adamw -- the clip of clip_grad_norm (norm, nonfinite flag,
+ * decision; max_norm, inv_scale, out_norm, out_nonfinite_flag and stream as
+ * there), then, unless the decision is SKIP, one AdamW step of optimizer
+ * step number `step` (1-based) on every element, with g^ = x * the clip's
+ * multiplier.  The gradients are read, not rewritten (set to +0 if
+ * p->zero_grads).  On SKIP nothing at all is written except the record,
+ * out_norm and out_nonfinite_flag.  Always runs as two launches (the split
+ * variant's norm pass, then the AdamW pass), whatever clip_set_variant chose.
+ * Asynchronous, no allocation.  Returns GCLIP_OK; GCLIP_ERR_INVALID_ARG
+ * (NULL handle or p, no state attached, bad max_norm / inv_scale, lr < 0,
+ * beta outside [0, 1), eps <= 0, weight_decay < 0, step < 1, or any of them
+ * not finite); GCLIP_ERR_CUDA if a launch failed. */
+int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
+                         const clip_adamw_params_t *p, int64_t step,
+                         float *out_norm, int32_t *out_nonfinite_flag,
+                         void *stream);
+
 /* clip_grad_norm_flat_noalloc -- the same clip for one contiguous gradient
  * buffer, for callers that cannot allocate device memory.
  *
