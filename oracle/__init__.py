@@ -125,6 +125,10 @@ class Oracle:
                                         ctypes.c_int32, ctypes.c_double, ctypes.c_double,
                                         ctypes.POINTER(_AdamwParams), ctypes.POINTER(_Result)]
         L.oracle_clip_adamw.restype = ctypes.c_int
+        L.oracle_clip_to_f32.argtypes = [ctypes.POINTER(_Tensor), ctypes.POINTER(ctypes.c_void_p),
+                                         ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+                                         ctypes.POINTER(_Result)]
+        L.oracle_clip_to_f32.restype = ctypes.c_int
         L.oracle_sumsq.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int32,
                                    ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_int32)]
@@ -178,6 +182,20 @@ class Oracle:
             raise ValueError("oracle_clip_sample rejected its arguments")
         return slots, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
                                    res.decision)
+
+    def clip_to_f32(self, tensors, max_norm: float, inv_scale: float = 1.0, fill=np.nan):
+        """Out-of-place clip into new float32 arrays (left at `fill` on
+        SKIP); returns (outputs, OracleResult)."""
+        outs = [np.full(t.data.size, fill, dtype=np.float32) for t in tensors]
+        ptrs = (ctypes.c_void_p * max(1, len(outs)))(*[o.ctypes.data if o.size else None
+                                                        for o in outs])
+        res = _Result()
+        rc = self._lib.oracle_clip_to_f32(self._descs(tensors), ptrs, len(tensors),
+                                          float(max_norm), float(inv_scale), ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_clip_to_f32 rejected its arguments")
+        return outs, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
+                                  res.decision)
 
     def clip_adamw(self, tensors, states, max_norm: float, inv_scale: float = 1.0, *,
                    lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,

@@ -395,6 +395,30 @@ int oracle_clip_sample(const oracle_tensor *in, int32_t n_tensors,
     return 0;
 }
 
+/* Out-of-place clip into fp32 buffers: the same decision as oracle_clip, and
+ * every element x becomes round_fp32(x * inv_scale * coef) in out[t] (fp32
+ * host arrays of the tensors' numel); on SKIP the outputs are not written.
+ * The gradients are not modified.  For fp16/bf16 gradients under loss
+ * scaling this keeps the unscaled values that binary16 could only hold as
+ * subnormals (the glossary page, "Order changes the result": unscale before
+ * the threshold; the backprop page, "Where gradients live": FP16 gradient
+ * buffers). */
+int oracle_clip_to_f32(const oracle_tensor *in, void *const *out,
+                       int32_t n_tensors, double max_norm, double inv_scale,
+                       oracle_result *res)
+{
+    if (decide(in, n_tensors, max_norm, inv_scale, res) != 0)
+        return -1;
+    if (res->decision == OR_DECISION_SKIP)
+        return 0;
+    for (int32_t t = 0; t < n_tensors; ++t)
+        for (int64_t i = 0; i < in[t].numel; ++i) {
+            double x = oracle_decode(in[t].data, i, in[t].dtype);
+            oracle_encode(out[t], i, OR_F32, clipped_value(x, inv_scale, res->coef));
+        }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Clip, then one AdamW step on the clipped gradients.
  *

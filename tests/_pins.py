@@ -366,6 +366,40 @@ def pin_sampled_outputs_match_full_clip(o):
         assert np.array_equal(got, want)
 
 
+# -- out-of-place fp32 output ---------------------------------------------------
+
+def pin_to_f32_matches_in_place_for_fp32(o):
+    """For fp32 gradients the out-of-place fp32 result is the in-place result
+    bit for bit (same decision, one rounding into the same format)."""
+    rng = np.random.default_rng(31)
+    ts = [make(rng.normal(0, 1, n), "f32") for n in (50, 3, 17)]
+    for c, s_ in ((2.0, 1.0), (100.0, 0.25), (0.5, 0.3)):
+        a, ra = o.clip(ts, c, s_)
+        b, rb = o.clip_to_f32(ts, c, s_)
+        assert ra.decision == rb.decision and ra.norm == rb.norm
+        for x, y in zip(a, b):
+            assert np.array_equal(x.data.view(np.int32), y.view(np.int32))
+
+
+def pin_to_f32_keeps_what_fp16_loses(o):
+    """Unscaling fp16 gradients by 2^-18 lands in the fp16 subnormal range:
+    in place, 0x3fff (1.999...) x 2^-18 must round to 128 x 2^-24; the fp32
+    output holds the exact value.  Both sides agree on the decision."""
+    raw = OracleTensor(np.array([0x3FFF, 0x3C00, 0xBFFF], np.uint16).view(np.float16), "f16")
+    s_ = 2.0 ** -18
+    inplace, r1 = o.clip([raw], 1.0, s_)
+    out, r2 = o.clip_to_f32([raw], 1.0, s_)
+    assert r1.decision == r2.decision == PASS
+    exact = as_float64(raw) * s_
+    assert np.array_equal(out[0].astype(np.float64), exact)
+    assert as_float64(inplace[0])[0] == 128 * 2.0 ** -24 != exact[0]
+
+
+def pin_to_f32_skip_writes_nothing(o):
+    out, r = o.clip_to_f32([make([1.0, math.inf], "bf16")], 1.0, fill=7.0)
+    assert r.decision == SKIP and np.all(out[0] == 7.0)
+
+
 # -- clip, then AdamW (the clipping page, "Order matters: Pre-Adam") ----------
 
 def _adamw_case(seed, sizes=(37, 5), dt="f32", scale=1e-3):
