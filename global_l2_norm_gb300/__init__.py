@@ -116,6 +116,27 @@ class GradClipper:
             out_flag.data_ptr(), _stream_handle(stream, self.device)))
         return out_norm, out_flag
 
+    # -- out-of-place fp32 output ---------------------------------------------
+    def attach_f32_out(self, outs) -> None:
+        """Attach fp32 CUDA tensors, one per gradient tensor (same numel), to
+        receive clip_to_f32_'s results.  They stay owned by the caller."""
+        outs = list(outs)
+        arr = (ctypes.c_void_p * max(1, len(outs)))()
+        for i, o in enumerate(outs):
+            if o.dtype != torch.float32 or not o.is_contiguous() or o.device != self.device:
+                raise ValueError("outputs must be contiguous fp32 on the gradients' device")
+            arr[i] = o.data_ptr() if o.numel() else None
+        self._outs = outs
+        check("clip_attach_f32_out", self._lib.clip_attach_f32_out(self._h, arr, len(outs)))
+
+    def clip_to_f32_(self, max_norm: float, inv_scale: float = 1.0, stream=None):
+        """Clip into the attached fp32 outputs; the gradients are only read.
+        Returns (norm, flag) device tensors."""
+        check("clip_grad_norm_to_f32", self._lib.clip_grad_norm_to_f32(
+            self._h, float(max_norm), float(inv_scale), self.norm.data_ptr(),
+            self.flag.data_ptr(), _stream_handle(stream, self.device)))
+        return self.norm, self.flag
+
     # -- fused clip + AdamW --------------------------------------------------
     def attach_adamw(self, states) -> None:
         """Attach fp32 (w, m, v) CUDA tensors, one triple per gradient tensor

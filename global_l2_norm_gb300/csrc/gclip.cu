@@ -678,6 +678,57 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const clip_chunk_t* __restri
 }
 
 // ---------------------------------------------------------------------------
+// Out-of-place clip into fp32: after the norm pass, every element is written
+// to its fp32 output as x * (chi + clo), rounded once.
+
+template <int DT>
+__device__ __forceinline__ void to_f32_chunk(const clip_chunk_t& c, const TensorState& ts, float chi,
+                                             float clo) {
+  constexpr uint32_t E = Fmt<DT>::kPerVec, B = Fmt<DT>::kBytes;
+  const Span sp = make_span<DT>(c.addr, c.numel);
+  const uint64_t e0 = (c.addr - ts.g) / B;
+  float* out = reinterpret_cast<float*>(ts.w) + e0;
+  const uint64_t pol = policy_evict_first();
+  const uint4* gv = reinterpret_cast<const uint4*>(sp.body);
+  if ((reinterpret_cast<uint64_t>(out + sp.head) & 15u) == 0) {
+    for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) {
+      float x[8];
+      widen_vec<DT>(HintMem::ld_scale(gv + i, pol), x);
+      float4* o = reinterpret_cast<float4*>(out + sp.head + i * E);
+#pragma unroll
+      for (uint32_t q = 0; q < E; q += 4)
+        __stcs(o + q / 4, make_float4(Fmt<GCLIP_F32>::scale1(x[q], chi, clo),
+                                      Fmt<GCLIP_F32>::scale1(x[q + 1], chi, clo),
+                                      Fmt<GCLIP_F32>::scale1(x[q + 2], chi, clo),
+                                      Fmt<GCLIP_F32>::scale1(x[q + 3], chi, clo)));
+    }
+  } else {
+    for (uint32_t j = sp.head + threadIdx.x; j < sp.tail_start; j += kThreads)
+      out[j] = Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(c.addr + static_cast<uint64_t>(j) * B), chi, clo);
+  }
+  for (uint32_t j = threadIdx.x; j < sp.head + sp.ntail; j += kThreads) {
+    const uint32_t k = j < sp.head ? j : sp.tail_start + (j - sp.head);
+    out[k] = Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(c.addr + static_cast<uint64_t>(k) * B), chi, clo);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_to_f32(const clip_chunk_t* __restrict__ chunks,
+                                                     int64_t n_chunks,
+                                                     const TensorState* __restrict__ outs,
+                                                     const clip_result_t* res) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (__ldcg(&res->decision) == GCLIP_DECISION_SKIP) return;
+  const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const TensorState ts = outs[c.meta >> 8];
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: to_f32_chunk<GCLIP_F32>(c, ts, chi, clo); break;
+    case GCLIP_F16: to_f32_chunk<GCLIP_F16>(c, ts, chi, clo); break;
+    default: to_f32_chunk<GCLIP_BF16>(c, ts, chi, clo); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Single-launch variant (cooperative launch, so every block is resident).
 
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
@@ -1196,6 +1247,7 @@ struct gclip_handle {
   SyncWords* d_sync;
   std::vector<clip_tensor_desc_t> descs;   // the gradient tensors, as created
   gclip::TensorState* d_states;            // AdamW state table (NULL until attached)
+  gclip::TensorState* d_outs;              // fp32 output table (NULL until attached)
 };
 
 namespace {
@@ -1461,6 +1513,7 @@ extern "C" int clip_destroy(clip_handle_t h) {
     if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) rc = GCLIP_ERR_CUDA;
     if (cudaFree(h->arena) != cudaSuccess) rc = GCLIP_ERR_CUDA;
     if (h->d_states != nullptr && cudaFree(h->d_states) != cudaSuccess) rc = GCLIP_ERR_CUDA;
+    if (h->d_outs != nullptr && cudaFree(h->d_outs) != cudaSuccess) rc = GCLIP_ERR_CUDA;
     cudaGetLastError();
   }
   delete h;
@@ -1533,22 +1586,28 @@ extern "C" int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals, int64
   return GCLIP_OK;
 }
 
-extern "C" int clip_attach_adamw(clip_handle_t h, const clip_adamw_state_t* states,
-                                 int32_t n_tensors) {
+namespace {
+
+// Validate per-tensor fp32 arrays (`per` of them for each tensor, `ptrs`
+// laid out tensor by tensor) against the handle's gradients, and replace
+// *slot with a device table of {gradient base, arrays...}.
+int attach_table(clip_handle_t h, const float* const* ptrs, int per, int32_t n_tensors,
+                 gclip::TensorState** slot) {
   if (h == nullptr || n_tensors != static_cast<int32_t>(h->descs.size()) ||
-      (n_tensors > 0 && states == nullptr))
+      (n_tensors > 0 && ptrs == nullptr))
     return GCLIP_ERR_INVALID_ARG;
-  std::vector<clip_tensor_desc_t> all(h->descs);  // gradients, then w, m, v of each tensor
+  std::vector<clip_tensor_desc_t> all(h->descs);  // gradients, then every array
   std::vector<gclip::TensorState> table(static_cast<size_t>(n_tensors));
   for (int32_t t = 0; t < n_tensors; ++t) {
     const clip_tensor_desc_t& d = h->descs[t];
+    uint64_t* f = &table[t].w;
     table[t].g = reinterpret_cast<uint64_t>(d.ptr);
-    table[t].w = reinterpret_cast<uint64_t>(states[t].w);
-    table[t].m = reinterpret_cast<uint64_t>(states[t].m);
-    table[t].v = reinterpret_cast<uint64_t>(states[t].v);
-    if (d.numel == 0) continue;
-    for (float* a : {states[t].w, states[t].m, states[t].v}) {
-      clip_tensor_desc_t s = {a, d.numel, GCLIP_F32, 0};
+    table[t].w = table[t].m = table[t].v = 0;
+    for (int k = 0; k < per; ++k) {
+      const float* a = ptrs[static_cast<size_t>(t) * per + k];
+      f[k] = reinterpret_cast<uint64_t>(a);
+      if (d.numel == 0) continue;
+      clip_tensor_desc_t s = {const_cast<float*>(a), d.numel, GCLIP_F32, 0};
       all.push_back(s);
     }
   }
@@ -1571,12 +1630,71 @@ extern "C" int clip_attach_adamw(clip_handle_t h, const clip_adamw_state_t* stat
     cudaFree(d);
     return GCLIP_ERR_CUDA;
   }
-  if (h->d_states != nullptr) {
+  if (*slot != nullptr) {
     cudaDeviceSynchronize();  // the old table may still be read by queued work
-    cudaFree(h->d_states);
+    cudaFree(*slot);
   }
-  h->d_states = d;
+  *slot = d;
   return GCLIP_OK;
+}
+
+// The split norm pass followed by one per-chunk kernel `fn` launched with
+// programmatic dependent launch on `args` (after the norm pass's own).
+int enqueue_norm_then(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
+                      int32_t* out_flag, cudaStream_t s, const void* fn, void** args) {
+  int64_t nc = h->n_chunks;
+  cudaError_t e = cudaSuccess;
+  if (nc == 0) {
+    const float2* partials = h->d_partials;
+    void* a[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm, &out_flag};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a, false);
+  } else {
+    gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag, 0);
+    void* a1[] = {&a};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial),
+                   static_cast<unsigned int>(h->grid_persistent), s, a1, false);
+    if (e == cudaSuccess) e = launch_pdl(fn, static_cast<unsigned int>(nc), s, args, true);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  return GCLIP_OK;
+}
+
+}  // namespace
+
+extern "C" int clip_attach_adamw(clip_handle_t h, const clip_adamw_state_t* states,
+                                 int32_t n_tensors) {
+  if (h == nullptr || (n_tensors > 0 && states == nullptr)) return GCLIP_ERR_INVALID_ARG;
+  std::vector<const float*> ptrs;
+  for (int32_t t = 0; t < n_tensors; ++t) {
+    ptrs.push_back(states[t].w);
+    ptrs.push_back(states[t].m);
+    ptrs.push_back(states[t].v);
+  }
+  return attach_table(h, ptrs.data(), 3, n_tensors, &h->d_states);
+}
+
+extern "C" int clip_attach_f32_out(clip_handle_t h, float* const* outs, int32_t n_tensors) {
+  if (h == nullptr) return GCLIP_ERR_INVALID_ARG;
+  return attach_table(h, const_cast<const float* const*>(outs), 1, n_tensors, &h->d_outs);
+}
+
+extern "C" int clip_grad_norm_to_f32(clip_handle_t h, float max_norm, float inv_scale,
+                                     float* out_norm, int32_t* out_nonfinite_flag, void* stream) {
+  if (h == nullptr || h->d_outs == nullptr || !valid_scalar(max_norm) || !valid_scalar(inv_scale))
+    return GCLIP_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  int64_t nc = h->n_chunks;
+  const clip_chunk_t* chunks = h->d_chunks;
+  const gclip::TensorState* outs = h->d_outs;
+  const clip_result_t* cres = h->d_result;
+  void* args[] = {&chunks, &nc, &outs, &cres};
+  return enqueue_norm_then(h, max_norm, inv_scale, out_norm, out_nonfinite_flag,
+                           static_cast<cudaStream_t>(stream),
+                           reinterpret_cast<const void*>(gclip::k_to_f32), args);
 }
 
 extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
@@ -1591,45 +1709,26 @@ extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_s
   if (!ok) return GCLIP_ERR_INVALID_ARG;
   DeviceGuard guard(h->device);
   if (!guard.ok) return GCLIP_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  gclip::AdamwArgs q;
+  const double b1 = p->beta1, b2 = p->beta2;
+  q.beta1 = p->beta1;
+  q.beta2 = p->beta2;
+  q.omb1 = static_cast<float>(1.0 - b1);
+  q.omb2 = static_cast<float>(1.0 - b2);
+  q.inv_bc1 = static_cast<float>(1.0 / (1.0 - std::pow(b1, static_cast<double>(step))));
+  q.inv_bc2 = static_cast<float>(1.0 / (1.0 - std::pow(b2, static_cast<double>(step))));
+  q.eps = p->eps;
+  q.lr = p->lr;
+  q.decay = static_cast<float>(1.0 - static_cast<double>(p->lr) * p->weight_decay);
+  q.zero_grads = p->zero_grads ? 1 : 0;
   int64_t nc = h->n_chunks;
-  cudaError_t e = cudaSuccess;
-  if (nc == 0) {
-    const float2* partials = h->d_partials;
-    void* args[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm,
-                    &out_nonfinite_flag};
-    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, args, false);
-  } else {
-    gclip::NormArgs a =
-        norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_nonfinite_flag, 0);
-    void* a1[] = {&a};
-    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial),
-                   static_cast<unsigned int>(h->grid_persistent), s, a1, false);
-    gclip::AdamwArgs q;
-    const double b1 = p->beta1, b2 = p->beta2;
-    q.beta1 = p->beta1;
-    q.beta2 = p->beta2;
-    q.omb1 = static_cast<float>(1.0 - b1);
-    q.omb2 = static_cast<float>(1.0 - b2);
-    q.inv_bc1 = static_cast<float>(1.0 / (1.0 - std::pow(b1, static_cast<double>(step))));
-    q.inv_bc2 = static_cast<float>(1.0 / (1.0 - std::pow(b2, static_cast<double>(step))));
-    q.eps = p->eps;
-    q.lr = p->lr;
-    q.decay = static_cast<float>(1.0 - static_cast<double>(p->lr) * p->weight_decay);
-    q.zero_grads = p->zero_grads ? 1 : 0;
-    const clip_chunk_t* chunks = h->d_chunks;
-    const gclip::TensorState* st = h->d_states;
-    const clip_result_t* cres = h->d_result;
-    void* a2[] = {&chunks, &nc, &st, &cres, &q};
-    if (e == cudaSuccess)
-      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_adamw), static_cast<unsigned int>(nc), s,
-                     a2, true);
-  }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return GCLIP_ERR_CUDA;
-  }
-  return GCLIP_OK;
+  const clip_chunk_t* chunks = h->d_chunks;
+  const gclip::TensorState* st = h->d_states;
+  const clip_result_t* cres = h->d_result;
+  void* args[] = {&chunks, &nc, &st, &cres, &q};
+  return enqueue_norm_then(h, max_norm, inv_scale, out_norm, out_nonfinite_flag,
+                           static_cast<cudaStream_t>(stream),
+                           reinterpret_cast<const void*>(gclip::k_adamw), args);
 }
 
 // ===========================================================================

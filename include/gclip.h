@@ -329,6 +329,35 @@ int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
                          float *out_norm, int32_t *out_nonfinite_flag,
                          void *stream);
 
+/* ---- out-of-place clip into fp32 ----------------------------------------
+ *
+ * For fp16/bf16 gradients kept under loss scaling: the unscaled values
+ * (the glossary page, "Order changes the result": unscale before the
+ * threshold) are often below binary16's normal range, where an in-place
+ * result can only keep a few bits.  This writes the clipped, unscaled
+ * gradients as fp32 into separate buffers (master gradients) and leaves the
+ * originals as they were. */
+
+/* clip_attach_f32_out -- outs[i] receives descriptor i's result: an fp32
+ * device array of the same numel, aligned to 4 bytes (16 lets the kernel
+ * use vector stores), not overlapping any gradient or other output.  Empty
+ * tensors may have NULL.  Copies a table of pointers to the device (the only
+ * allocation).  Returns GCLIP_OK, GCLIP_ERR_INVALID_ARG, GCLIP_ERR_OOM or
+ * GCLIP_ERR_CUDA. */
+int clip_attach_f32_out(clip_handle_t h, float *const *outs, int32_t n_tensors);
+
+/* clip_grad_norm_to_f32 -- the norm, flag and decision of clip_grad_norm;
+ * then, unless the decision is SKIP, every element x is written to its
+ * output as x * multiplier (inv_scale * max_norm / norm, or inv_scale)
+ * rounded once to fp32, even when the multiplier is 1.  The gradients are
+ * only read.  Two launches (the split norm pass, then the conversion),
+ * whatever clip_set_variant chose; asynchronous, no allocation.  Returns
+ * GCLIP_OK; GCLIP_ERR_INVALID_ARG (NULL handle, no outputs attached, bad
+ * max_norm / inv_scale); GCLIP_ERR_CUDA. */
+int clip_grad_norm_to_f32(clip_handle_t h, float max_norm, float inv_scale,
+                          float *out_norm, int32_t *out_nonfinite_flag,
+                          void *stream);
+
 /* clip_grad_norm_flat_noalloc -- the same clip for one contiguous gradient
  * buffer, for callers that cannot allocate device memory.
  *
