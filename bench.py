@@ -56,6 +56,8 @@ def parse_args(argv=None):
                    help="one set, no L2 flush (only for workloads that write nothing)")
     p.add_argument("--graph", action="store_true",
                    help="replay each run of clips as one captured CUDA graph")
+    p.add_argument("--per-tensor", action="store_true",
+                   help="clip each tensor by its own norm (clip_grad_norm_per_tensor)")
     p.add_argument("--adamw", action="store_true",
                    help="time the fused clip + AdamW step instead of the clip alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -316,6 +318,12 @@ def run_gclip(args):
 
     writes = True
 
+    def clip(c):
+        if args.per_tensor:
+            c.clip_per_tensor_(w.max_norm, w.inv_scale)
+        else:
+            c.clip_(w.max_norm, w.inv_scale)
+
     def restore():
         # a clip that wrote changed its input: put the pristine values back
         if writes:
@@ -327,28 +335,37 @@ def run_gclip(args):
     # correctness of the step being timed: the decision and a norm that agrees
     # with a float64 torch norm of the same data (a sanity check, not parity)
     restore()
-    clippers[0].clip_(w.max_norm, w.inv_scale)
-    rec = clippers[0].result()
-    ref_norm = math.sqrt(sum(float(t.double().square().sum()) for t in pristine.tensors)
-                         ) * w.inv_scale
-    if math.isfinite(ref_norm):
-        assert abs(rec["norm"] - ref_norm) <= 1e-5 * ref_norm, (rec["norm"], ref_norm)
+    clip(clippers[0])
+    if args.per_tensor:
+        recs = clippers[0].per_tensor_results()
+        wr = [r["decision"] != g.GCLIP_DECISION_SKIP and not (
+            r["coef_hi"] == 1.0 and r["coef_lo"] == 0.0) for r in recs]
+        writes = any(wr)
+        written = sum(s_.numel for s_, x in zip(w.layout, wr) if x)
+        rec = {"decision": g.GCLIP_DECISION_CLIP if writes else g.GCLIP_DECISION_PASS}
     else:
-        assert rec["nonfinite"] == 1, rec
-    writes = rec["decision"] != g.GCLIP_DECISION_SKIP and not (
-        rec["coef_hi"] == 1.0 and rec["coef_lo"] == 0.0)
+        rec = clippers[0].result()
+        ref_norm = math.sqrt(sum(float(t.double().square().sum()) for t in pristine.tensors)
+                             ) * w.inv_scale
+        if math.isfinite(ref_norm):
+            assert abs(rec["norm"] - ref_norm) <= 1e-5 * ref_norm, (rec["norm"], ref_norm)
+        else:
+            assert rec["nonfinite"] == 1, rec
+        writes = rec["decision"] != g.GCLIP_DECISION_SKIP and not (
+            rec["coef_hi"] == 1.0 and rec["coef_lo"] == 0.0)
+        written = w.numel if writes else 0
     if args.warm and writes:
         print(json.dumps({"error": "--warm needs a workload whose clip writes nothing"}))
         return 2
     decision_name = {0: "pass", 1: "clip", 2: "skip"}[rec["decision"]]
-    nbytes = algorithmic_bytes(w.numel, w.elem_bytes, "write" if writes else "read")
+    nbytes = w.numel * w.elem_bytes + 2 * written * w.elem_bytes
 
     # warm-up
     restore()
     for i in range(args.warmup):
         if i and i % P == 0:
             restore()
-        clippers[i % P].clip_(w.max_norm, w.inv_scale)
+        clip(clippers[i % P])
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -368,13 +385,13 @@ def run_gclip(args):
     def run_clips(n):
         if not args.graph:
             for i in range(n):
-                clippers[i % P].clip_(w.max_norm, w.inv_scale)
+                clip(clippers[i % P])
             return
         if n not in graphs:
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr):
                 for i in range(n):
-                    clippers[i % P].clip_(w.max_norm, w.inv_scale)
+                    clip(clippers[i % P])
             graphs[n] = gr
             restore()
             torch.cuda.synchronize()
@@ -505,7 +522,8 @@ def run_gclip(args):
             "config": {
                 "workload": w.name, "description": w.description, "tensors": len(w.layout),
                 "elements": w.numel, "bytes_per_step": nbytes, "decision": decision_name,
-                "variant": args.variant, "pool": P, "l2_keep_mb": args.l2_keep_mb, "parallelism": f"replicas x{world}",
+                "variant": "per_tensor" if args.per_tensor else args.variant, "pool": P,
+                "l2_keep_mb": args.l2_keep_mb, "written_elements": written, "parallelism": f"replicas x{world}",
                 "l2": ("warm: one set re-read from L2, no flush" if args.warm else
                        "inputs larger than L2 (one set per step, pool of distinct sets); "
                        "L2 flushed before each timed run"),

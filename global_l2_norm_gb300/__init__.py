@@ -116,6 +116,27 @@ class GradClipper:
             out_flag.data_ptr(), _stream_handle(stream, self.device)))
         return out_norm, out_flag
 
+    # -- per-tensor clipping ---------------------------------------------------
+    def clip_per_tensor_(self, max_norm: float, inv_scale: float = 1.0, stream=None):
+        """Clip every tensor by its own norm, in place.  Returns device tensors
+        of the per-tensor norms (float32[n]) and nonfinite flags (int32[n])."""
+        n = len(self.tensors)
+        if getattr(self, "_pt_norms", None) is None:
+            self._pt_norms = torch.zeros(max(1, n), dtype=torch.float32, device=self.device)
+            self._pt_flags = torch.zeros(max(1, n), dtype=torch.int32, device=self.device)
+        check("clip_grad_norm_per_tensor", self._lib.clip_grad_norm_per_tensor(
+            self._h, float(max_norm), float(inv_scale), self._pt_norms.data_ptr(),
+            self._pt_flags.data_ptr(), _stream_handle(stream, self.device)))
+        return self._pt_norms[:n], self._pt_flags[:n]
+
+    def per_tensor_results(self, stream=None) -> list:
+        n = len(self.tensors)
+        recs = (clip_result_t * max(1, n))()
+        check("clip_read_per_tensor", self._lib.clip_read_per_tensor(
+            self._h, recs, n, _stream_handle(stream, self.device)))
+        return [{k: getattr(r, k) for k, _ in clip_result_t._fields_ if k != "reserved"}
+                for r in recs[:n]]
+
     # -- out-of-place fp32 output ---------------------------------------------
     def attach_f32_out(self, outs) -> None:
         """Attach fp32 CUDA tensors, one per gradient tensor (same numel), to

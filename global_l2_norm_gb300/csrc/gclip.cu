@@ -410,12 +410,10 @@ __device__ __forceinline__ bool must_write(int decision, float chi, float clo) {
 // operations, and the multiplier inv_scale * max_norm / norm is handed to the
 // scaling pass as a float-float pair so that each output is rounded once.
 
-__device__ void final_reduce(const float2* partials, int64_t n_chunks, float max_norm,
-                             float inv_scale, clip_result_t* res, float* out_norm,
-                             int32_t* out_flag, FF* red) {
+__device__ FF reduce_partials(const float2* partials, int64_t n, FF* red) {
   FF acc = {0.f, 0.f};
   int64_t c = threadIdx.x;
-  for (; c + 3 * kThreads < n_chunks; c += 4 * kThreads) {
+  for (; c + 3 * kThreads < n; c += 4 * kThreads) {
     const float2 p0 = __ldcg(partials + c);
     const float2 p1 = __ldcg(partials + c + kThreads);
     const float2 p2 = __ldcg(partials + c + 2 * kThreads);
@@ -425,13 +423,17 @@ __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max
     acc = ff_add(acc, FF{p2.x, p2.y});
     acc = ff_add(acc, FF{p3.x, p3.y});
   }
-  for (; c < n_chunks; c += kThreads) {
+  for (; c < n; c += kThreads) {
     const float2 p = __ldcg(partials + c);
     acc = ff_add(acc, FF{p.x, p.y});
   }
-  acc = block_reduce(acc, red);
-  if (threadIdx.x != 0) return;
+  return block_reduce(acc, red);
+}
 
+// The norm, flag, decision and multiplier from the float-float sum of
+// squares S = hi + lo (thread 0).
+__device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_result_t* res,
+                             float* out_norm, int32_t* out_flag) {
   const double S = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
   const bool nonfinite = !isfinite(acc.hi) || !isfinite(acc.lo) || S > static_cast<double>(FLT_MAX);
   const double norm = sqrt(S);
@@ -459,6 +461,13 @@ __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max
   res->calls = res->calls + 1u;
   if (out_norm) *out_norm = norm_f;
   if (out_flag) *out_flag = nonfinite ? 1 : 0;
+}
+
+__device__ void final_reduce(const float2* partials, int64_t n_chunks, float max_norm,
+                             float inv_scale, clip_result_t* res, float* out_norm,
+                             int32_t* out_flag, FF* red) {
+  const FF acc = reduce_partials(partials, n_chunks, red);
+  if (threadIdx.x == 0) decide_write(acc, max_norm, inv_scale, res, out_norm, out_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -726,6 +735,48 @@ __global__ void __launch_bounds__(kThreads) k_to_f32(const clip_chunk_t* __restr
     case GCLIP_F16: to_f32_chunk<GCLIP_F16>(c, ts, chi, clo); break;
     default: to_f32_chunk<GCLIP_BF16>(c, ts, chi, clo); break;
   }
+}
+
+// ---------------------------------------------------------------------------
+// Per-tensor clipping: each tensor clipped by its own norm.  One block per
+// chunk writes the chunk's sum of squares; one block per tensor reduces its
+// chunks' sums (the same fixed order as the final reduction) and decides;
+// one block per chunk scales with its tensor's multiplier.
+
+__global__ void __launch_bounds__(kThreads) k_chunk_partials(const clip_chunk_t* __restrict__ chunks,
+                                                             float inv_scale,
+                                                             float2* __restrict__ partials) {
+  __shared__ FF red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const FF acc = chunk_sumsq<HintMem>(chunks[blockIdx.x], inv_scale, red, policy_evict_first());
+  if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
+}
+
+__global__ void __launch_bounds__(kThreads) k_tensor_final(const float2* __restrict__ partials,
+                                                           const int64_t* __restrict__ first,
+                                                           float max_norm, float inv_scale,
+                                                           clip_result_t* recs, float* out_norms,
+                                                           int32_t* out_flags) {
+  __shared__ FF red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int t = blockIdx.x;
+  const FF acc = reduce_partials(partials + first[t], first[t + 1] - first[t], red);
+  if (threadIdx.x == 0)
+    decide_write(acc, max_norm, inv_scale, recs + t, out_norms ? out_norms + t : nullptr,
+                 out_flags ? out_flags + t : nullptr);
+}
+
+__global__ void __launch_bounds__(kThreads) k_scale_per_tensor(const clip_chunk_t* __restrict__ chunks,
+                                                               int64_t n_chunks,
+                                                               const clip_result_t* recs) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const clip_result_t* r = recs + (c.meta >> 8);
+  const int decision = __ldcg(&r->decision);
+  const float chi = __ldcg(&r->coef_hi), clo = __ldcg(&r->coef_lo);
+  if (!must_write(decision, chi, clo)) return;
+  chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
 }
 
 // ---------------------------------------------------------------------------
@@ -1245,6 +1296,8 @@ struct gclip_handle {
   float2* d_partials;        // one entry per block of the norm pass (G)
   clip_result_t* d_result;
   SyncWords* d_sync;
+  int64_t* d_first;          // first chunk of each tensor, n_tensors + 1 entries
+  clip_result_t* d_trec;     // per-tensor records of clip_grad_norm_per_tensor
   std::vector<clip_tensor_desc_t> descs;   // the gradient tensors, as created
   gclip::TensorState* d_states;            // AdamW state table (NULL until attached)
   gclip::TensorState* d_outs;              // fp32 output table (NULL until attached)
@@ -1338,7 +1391,19 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   const size_t off_partials = round_up(off_chunks + n * sizeof(clip_chunk_t), 256);
   const size_t off_result = round_up(off_partials + n * sizeof(float2), 256);
   const size_t off_sync = round_up(off_result + sizeof(clip_result_t), 256);
-  const size_t total = round_up(off_sync + sizeof(SyncWords), 256);
+  const size_t nt = static_cast<size_t>(n_tensors);
+  const size_t off_first = round_up(off_sync + sizeof(SyncWords), 256);
+  const size_t off_trec = round_up(off_first + (nt + 1) * sizeof(int64_t), 256);
+  const size_t total = round_up(off_trec + (nt ? nt : 1) * sizeof(clip_result_t), 256);
+  std::vector<int64_t> first(nt + 1, 0);
+  {
+    size_t c = 0;
+    for (size_t t = 0; t < nt; ++t) {
+      first[t] = static_cast<int64_t>(c);
+      while (c < n && (chunks[c].meta >> 8) == t) ++c;
+    }
+    first[nt] = static_cast<int64_t>(c);
+  }
   cudaError_t e = cudaMalloc(&h->arena, total);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -1350,11 +1415,15 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   h->d_partials = reinterpret_cast<float2*>(base + off_partials);
   h->d_result = reinterpret_cast<clip_result_t*>(base + off_result);
   h->d_sync = reinterpret_cast<SyncWords*>(base + off_sync);
+  h->d_first = reinterpret_cast<int64_t*>(base + off_first);
+  h->d_trec = reinterpret_cast<clip_result_t*>(base + off_trec);
 
   int sms = 0, per_sm = 0, coop = 0, l2 = 0;
   e = cudaMemset(h->arena, 0, total);
   if (e == cudaSuccess && n > 0)
     e = cudaMemcpy(h->d_chunks, chunks.data(), n * sizeof(clip_chunk_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_first, first.data(), first.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device);
@@ -1729,6 +1798,59 @@ extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_s
   return enqueue_norm_then(h, max_norm, inv_scale, out_norm, out_nonfinite_flag,
                            static_cast<cudaStream_t>(stream),
                            reinterpret_cast<const void*>(gclip::k_adamw), args);
+}
+
+extern "C" int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float inv_scale,
+                                         float* out_norms, int32_t* out_nonfinite_flags,
+                                         void* stream) {
+  if (h == nullptr || !valid_scalar(max_norm) || !valid_scalar(inv_scale))
+    return GCLIP_ERR_INVALID_ARG;
+  const unsigned int nt = static_cast<unsigned int>(h->descs.size());
+  if (nt == 0) return GCLIP_OK;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t nc = h->n_chunks;
+  const clip_chunk_t* chunks = h->d_chunks;
+  float2* partials = h->d_partials;
+  const float2* cpartials = partials;
+  const int64_t* first = h->d_first;
+  clip_result_t* recs = h->d_trec;
+  const clip_result_t* crecs = recs;
+  cudaError_t e = cudaSuccess;
+  if (nc > 0) {
+    void* a1[] = {&chunks, &inv_scale, &partials};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_chunk_partials),
+                   static_cast<unsigned int>(nc), s, a1, false);
+  }
+  void* a2[] = {&cpartials, &first, &max_norm, &inv_scale, &recs, &out_norms, &out_nonfinite_flags};
+  if (e == cudaSuccess)
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_tensor_final), nt, s, a2, nc > 0);
+  void* a3[] = {&chunks, &nc, &crecs};
+  if (e == cudaSuccess && nc > 0)
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_scale_per_tensor),
+                   static_cast<unsigned int>(nc), s, a3, true);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  return GCLIP_OK;
+}
+
+extern "C" int clip_read_per_tensor(clip_handle_t h, clip_result_t* out, int32_t n, void* stream) {
+  if (h == nullptr || out == nullptr || n < 0 || n > static_cast<int32_t>(h->descs.size()))
+    return GCLIP_ERR_INVALID_ARG;
+  if (n == 0) return GCLIP_OK;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(out, h->d_trec, sizeof(clip_result_t) * n, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  return GCLIP_OK;
 }
 
 // ===========================================================================

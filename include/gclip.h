@@ -329,6 +329,34 @@ int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
                          float *out_norm, int32_t *out_nonfinite_flag,
                          void *stream);
 
+/* ---- per-tensor clipping -------------------------------------------------
+ *
+ * Source: the clipping page, section "Per-Tensor or Global": each gradient
+ * tensor clipped by its own norm, the simpler alternative that distorts the
+ * relative scales between tensors (the global clip above is what the page
+ * uses); the glossary page, "Shorten the arrow, keep the direction": a limit
+ * per layer is a different constraint. */
+
+/* clip_grad_norm_per_tensor -- for every tensor t of the handle on its own:
+ * norm_t of its unscaled elements, and x <- x * inv_scale * (norm_t > max_norm
+ * ? max_norm / norm_t : 1), nothing written when that multiplier is 1 or
+ * when tensor t holds a NaN/inf (that tensor alone is skipped).  Empty
+ * tensors have norm 0.  out_norms, out_nonfinite_flags: device arrays of one
+ * entry per tensor, each may be NULL.  The per-tensor records go to the
+ * handle (clip_read_per_tensor).  Three launches (chunk sums, one block per
+ * tensor, scaling); asynchronous, no allocation.  Returns GCLIP_OK,
+ * GCLIP_ERR_INVALID_ARG (NULL handle, bad max_norm / inv_scale) or
+ * GCLIP_ERR_CUDA. */
+int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float inv_scale,
+                              float *out_norms, int32_t *out_nonfinite_flags,
+                              void *stream);
+
+/* clip_read_per_tensor -- copy the first n per-tensor records of the last
+ * clip_grad_norm_per_tensor call to host memory `out`, synchronising
+ * `stream`.  Returns GCLIP_OK, GCLIP_ERR_INVALID_ARG (n < 0 or more than the
+ * handle's tensors, NULL arguments) or GCLIP_ERR_CUDA. */
+int clip_read_per_tensor(clip_handle_t h, clip_result_t *out, int32_t n, void *stream);
+
 /* ---- out-of-place clip into fp32 ----------------------------------------
  *
  * For fp16/bf16 gradients kept under loss scaling: the unscaled values

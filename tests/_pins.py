@@ -116,6 +116,21 @@ def pin_global_not_per_tensor(o):
     assert not np.array_equal(as_float64(pt[0]), ob)
 
 
+def pin_per_tensor_isolation(o):
+    """Per-tensor clipping treats each tensor alone (clipping page, "Per-Tensor
+    or Global"): a NaN in one tensor skips only that tensor, and each of the
+    others is scaled by its own max_norm / norm."""
+    a = make([6.0, 8.0], "f32")            # norm 10 -> [3, 4] at 5
+    b = make([1.0, math.nan], "f16")        # skipped, untouched
+    c = make([0.6, 0.8], "bf16")           # norm ~1 < 5: passes unchanged
+    outs, rs = o.clip_per_tensor([a, b, c], 5.0)
+    assert [r.decision for r in rs] == [CLIP, SKIP, PASS]
+    assert list(as_float64(outs[0])) == [3.0, 4.0]
+    assert np.array_equal(storage_bits(outs[1]), storage_bits(b))
+    assert np.array_equal(storage_bits(outs[2]), storage_bits(c))
+    assert rs[0].norm == 10.0 and not math.isfinite(rs[1].norm)
+
+
 def pin_post_clip_norm(o):
     """After a clip the new norm equals max_norm (clipping page, Mathematics);
     in fp32 storage, up to the rounding of each element."""
