@@ -423,7 +423,8 @@ def run_gclip(args):
     step_us = sorted(t / n * 1e3 for t, n in runs)
 
     # per-kernel durations for the roofline (events between the launches)
-    launches_per_step = 1 if args.variant.startswith("persistent") else 2
+    launches_per_step = 3 if args.per_tensor else (
+        1 if args.variant.startswith("persistent") else 2)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in evs:           # torch creates the CUDA event on its first record
         e.record(stream)
@@ -440,7 +441,9 @@ def run_gclip(args):
         for k in range(3):
             seg[k].append(evs[k].elapsed_time(evs[k + 1]))
     seg_ms = [statistics.mean(s) for s in seg]
-    if args.variant.startswith("persistent"):
+    if args.per_tensor:
+        kernel, k_bytes, k_ms = "per-tensor clip (3 launches, timed region)", nbytes, per_step_ms
+    elif args.variant.startswith("persistent"):
         kernel = "k_clip_persistent_tma" if args.variant.endswith("tma") else "k_clip_persistent"
         k_bytes, k_ms = nbytes, seg_ms[2]
         # the timed region is back-to-back launches of this one kernel
@@ -470,7 +473,7 @@ def run_gclip(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.per_tensor:
         host = pristine.flat.cpu().pin_memory()
         norm_h = torch.empty(1, dtype=torch.float32).pin_memory()
         flag_h = torch.empty(1, dtype=torch.int32).pin_memory()
