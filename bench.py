@@ -107,10 +107,12 @@ def aggregate(elapsed_ms: float, units: float, world: int, reduce_max=None):
 
 
 def source_digest() -> str:
+    """Digest of the library's sources (every file under csrc/)."""
     h = hashlib.sha256()
-    for f in ("gclip.cu", "plan.cpp", "internal.hpp"):
-        with open(os.path.join(ROOT, "global_l2_norm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    d = os.path.join(ROOT, "global_l2_norm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 

@@ -1,0 +1,337 @@
+// kernels.cuh -- the register-engine kernels: the split variant, fused clip
+// + AdamW, the out-of-place fp32 clip, per-tensor clipping and the
+// single-launch variant.  Included by gclip.cu only.
+#pragma once
+
+#include "reduce.cuh"
+
+namespace gclip {
+
+// ---------------------------------------------------------------------------
+// Split variant: the norm pass (with the final reduction in the last block)
+// and the scaling pass as two launches.
+
+__global__ void __launch_bounds__(kThreads) k_grad_norm_partial(const NormArgs a) {
+  __shared__ FF red[kWarps];
+  __shared__ int s_flag;
+  // Let the dependent scaling launch be scheduled while this grid runs.
+  asm volatile("griddepcontrol.launch_dependents;");
+  const FF bsum = block_norm_pass(a, red);
+  norm_arrive(a, bsum, red, &s_flag);
+}
+
+// One block of the final reduction alone: used when there are no chunks and
+// by the no-allocation entry point.
+__global__ void __launch_bounds__(kThreads) k_grad_norm_final(const float2* __restrict__ partials,
+                                                              int64_t n_chunks, float max_norm,
+                                                              float inv_scale, clip_result_t* res,
+                                                              float* out_norm, int32_t* out_flag) {
+  __shared__ FF red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  final_reduce(partials, n_chunks, max_norm, inv_scale, res, out_norm, out_flag, red);
+}
+
+__global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __restrict__ chunks,
+                                                         int64_t n_chunks,
+                                                         const clip_result_t* res) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int decision = res->decision;
+  const float chi = res->coef_hi, clo = res->coef_lo;
+  if (!must_write(decision, chi, clo)) return;
+  // Highest chunks first: the norm pass read them last and kept them in L2.
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
+}
+
+// ---------------------------------------------------------------------------
+// Fused clip + AdamW: after the norm pass, one pass over gradients and state
+// that forms the clipped gradient in registers and updates w, m, v.
+
+struct TensorState {
+  uint64_t g, w, m, v;  // gradient base and the fp32 state arrays of one tensor
+};
+
+struct AdamwArgs {
+  float beta1, beta2, omb1, omb2;  // beta and 1 - beta, each rounded once to fp32
+  float inv_bc1, inv_bc2;          // 1 / (1 - beta^step), from double
+  float eps, lr, decay;            // decay = 1 - lr * weight_decay, from double
+  int zero_grads;
+};
+
+// One element: g^ = x * (chi + clo) rounded once, then the moments and the
+// weight, each with IEEE-rounded fp32 operations.
+__device__ __forceinline__ void adamw1(float x, float& w, float& m, float& v, float chi, float clo,
+                                       const AdamwArgs& p) {
+  const float gh = __fmaf_rn(x, chi, __fmul_rn(x, clo));
+  m = __fmaf_rn(p.beta1, m, __fmul_rn(p.omb1, gh));
+  v = __fmaf_rn(p.beta2, v, __fmul_rn(p.omb2, __fmul_rn(gh, gh)));
+  const float denom = __fadd_rn(__fsqrt_rn(__fmul_rn(v, p.inv_bc2)), p.eps);
+  const float upd = __fdiv_rn(__fmul_rn(m, p.inv_bc1), denom);
+  w = __fmaf_rn(-p.lr, upd, __fmul_rn(w, p.decay));
+}
+
+__device__ __forceinline__ void adamw4(const float (&x)[4], float4* w, float4* m, float4* v, float chi,
+                                       float clo, const AdamwArgs& p) {
+  float4 W = __ldcs(w), M = __ldcs(m), V = __ldcs(v);
+  adamw1(x[0], W.x, M.x, V.x, chi, clo, p);
+  adamw1(x[1], W.y, M.y, V.y, chi, clo, p);
+  adamw1(x[2], W.z, M.z, V.z, chi, clo, p);
+  adamw1(x[3], W.w, M.w, V.w, chi, clo, p);
+  __stcs(w, W);
+  __stcs(m, M);
+  __stcs(v, V);
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_vec(uint4 g, float (&x)[8]) {
+  if constexpr (DT == GCLIP_F32) {
+    x[0] = __uint_as_float(g.x);
+    x[1] = __uint_as_float(g.y);
+    x[2] = __uint_as_float(g.z);
+    x[3] = __uint_as_float(g.w);
+  } else {
+    const float2 a = Fmt<DT>::widen(g.x), b = Fmt<DT>::widen(g.y), c = Fmt<DT>::widen(g.z),
+                 d = Fmt<DT>::widen(g.w);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void adamw_chunk(const clip_chunk_t& c, const TensorState& ts, float chi,
+                                            float clo, const AdamwArgs& p) {
+  constexpr uint32_t E = Fmt<DT>::kPerVec, B = Fmt<DT>::kBytes;
+  const Span sp = make_span<DT>(c.addr, c.numel);
+  const uint64_t e0 = (c.addr - ts.g) / B;  // index of the chunk's first element
+  float* w = reinterpret_cast<float*>(ts.w) + e0;
+  float* m = reinterpret_cast<float*>(ts.m) + e0;
+  float* v = reinterpret_cast<float*>(ts.v) + e0;
+  const uint64_t pol = policy_evict_first();
+  uint4* gv = reinterpret_cast<uint4*>(sp.body);
+  const bool vec = ((reinterpret_cast<uint64_t>(w + sp.head) | reinterpret_cast<uint64_t>(m + sp.head) |
+                     reinterpret_cast<uint64_t>(v + sp.head)) & 15u) == 0;
+  if (vec) {
+    for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) {
+      float x[8];
+      widen_vec<DT>(HintMem::ld_scale(gv + i, pol), x);
+      const uint32_t k = sp.head + i * E;
+#pragma unroll
+      for (uint32_t q = 0; q < E; q += 4) {
+        const float xs[4] = {x[q], x[q + 1], x[q + 2], x[q + 3]};
+        adamw4(xs, reinterpret_cast<float4*>(w + k + q), reinterpret_cast<float4*>(m + k + q),
+               reinterpret_cast<float4*>(v + k + q), chi, clo, p);
+      }
+      if (p.zero_grads) HintMem::st_scale(gv + i, make_uint4(0, 0, 0, 0), pol);
+    }
+  } else {
+    // state not 16-byte aligned with the gradient: element by element
+    for (uint32_t j = sp.head + threadIdx.x; j < sp.tail_start; j += kThreads) {
+      const uint64_t a = c.addr + static_cast<uint64_t>(j) * B;
+      float W = w[j], M = m[j], V = v[j];
+      adamw1(Fmt<DT>::load1(a), W, M, V, chi, clo, p);
+      w[j] = W;
+      m[j] = M;
+      v[j] = V;
+      if (p.zero_grads) Fmt<DT>::store1(a, 0.0f);
+    }
+  }
+  for (uint32_t j = threadIdx.x; j < sp.head + sp.ntail; j += kThreads) {
+    const uint32_t k = j < sp.head ? j : sp.tail_start + (j - sp.head);
+    const uint64_t a = c.addr + static_cast<uint64_t>(k) * B;
+    float W = w[k], M = m[k], V = v[k];
+    adamw1(Fmt<DT>::load1(a), W, M, V, chi, clo, p);
+    w[k] = W;
+    m[k] = M;
+    v[k] = V;
+    if (p.zero_grads) Fmt<DT>::store1(a, 0.0f);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_adamw(const clip_chunk_t* __restrict__ chunks,
+                                                    int64_t n_chunks,
+                                                    const TensorState* __restrict__ states,
+                                                    const clip_result_t* res, const AdamwArgs p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (__ldcg(&res->decision) == GCLIP_DECISION_SKIP) return;
+  const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
+  // Highest chunks first: the norm pass read their gradients last.
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const TensorState ts = states[c.meta >> 8];
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: adamw_chunk<GCLIP_F32>(c, ts, chi, clo, p); break;
+    case GCLIP_F16: adamw_chunk<GCLIP_F16>(c, ts, chi, clo, p); break;
+    default: adamw_chunk<GCLIP_BF16>(c, ts, chi, clo, p); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Out-of-place clip into fp32: after the norm pass, every element is written
+// to its fp32 output as x * (chi + clo), rounded once.
+
+template <int DT>
+__device__ __forceinline__ void to_f32_chunk(const clip_chunk_t& c, const TensorState& ts, float chi,
+                                             float clo) {
+  constexpr uint32_t E = Fmt<DT>::kPerVec, B = Fmt<DT>::kBytes;
+  const Span sp = make_span<DT>(c.addr, c.numel);
+  const uint64_t e0 = (c.addr - ts.g) / B;
+  float* out = reinterpret_cast<float*>(ts.w) + e0;
+  const uint64_t pol = policy_evict_first();
+  const uint4* gv = reinterpret_cast<const uint4*>(sp.body);
+  if ((reinterpret_cast<uint64_t>(out + sp.head) & 15u) == 0) {
+    for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) {
+      float x[8];
+      widen_vec<DT>(HintMem::ld_scale(gv + i, pol), x);
+      float4* o = reinterpret_cast<float4*>(out + sp.head + i * E);
+#pragma unroll
+      for (uint32_t q = 0; q < E; q += 4)
+        __stcs(o + q / 4, make_float4(Fmt<GCLIP_F32>::scale1(x[q], chi, clo),
+                                      Fmt<GCLIP_F32>::scale1(x[q + 1], chi, clo),
+                                      Fmt<GCLIP_F32>::scale1(x[q + 2], chi, clo),
+                                      Fmt<GCLIP_F32>::scale1(x[q + 3], chi, clo)));
+    }
+  } else {
+    for (uint32_t j = sp.head + threadIdx.x; j < sp.tail_start; j += kThreads)
+      out[j] = Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(c.addr + static_cast<uint64_t>(j) * B), chi, clo);
+  }
+  for (uint32_t j = threadIdx.x; j < sp.head + sp.ntail; j += kThreads) {
+    const uint32_t k = j < sp.head ? j : sp.tail_start + (j - sp.head);
+    out[k] = Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(c.addr + static_cast<uint64_t>(k) * B), chi, clo);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_to_f32(const clip_chunk_t* __restrict__ chunks,
+                                                     int64_t n_chunks,
+                                                     const TensorState* __restrict__ outs,
+                                                     const clip_result_t* res) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (__ldcg(&res->decision) == GCLIP_DECISION_SKIP) return;
+  const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const TensorState ts = outs[c.meta >> 8];
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: to_f32_chunk<GCLIP_F32>(c, ts, chi, clo); break;
+    case GCLIP_F16: to_f32_chunk<GCLIP_F16>(c, ts, chi, clo); break;
+    default: to_f32_chunk<GCLIP_BF16>(c, ts, chi, clo); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per-tensor clipping: each tensor clipped by its own norm.  One block per
+// chunk writes the chunk's sum of squares; one block per tensor reduces its
+// chunks' sums (the same fixed order as the final reduction) and decides;
+// one block per chunk scales with its tensor's multiplier.
+
+__global__ void __launch_bounds__(kThreads) k_chunk_partials(const clip_chunk_t* __restrict__ chunks,
+                                                             float inv_scale,
+                                                             float2* __restrict__ partials) {
+  __shared__ FF red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const FF acc = chunk_sumsq<HintMem>(chunks[blockIdx.x], inv_scale, red, policy_evict_first());
+  if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
+}
+
+__global__ void __launch_bounds__(kThreads) k_tensor_final(const float2* __restrict__ partials,
+                                                           const int64_t* __restrict__ first,
+                                                           float max_norm, float inv_scale,
+                                                           clip_result_t* recs, float* out_norms,
+                                                           int32_t* out_flags) {
+  __shared__ FF red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int t = blockIdx.x;
+  const FF acc = reduce_partials(partials + first[t], first[t + 1] - first[t], red);
+  if (threadIdx.x == 0)
+    decide_write(acc, max_norm, inv_scale, recs + t, out_norms ? out_norms + t : nullptr,
+                 out_flags ? out_flags + t : nullptr);
+}
+
+__global__ void __launch_bounds__(kThreads) k_scale_per_tensor(const clip_chunk_t* __restrict__ chunks,
+                                                               int64_t n_chunks,
+                                                               const clip_result_t* recs) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const clip_result_t* r = recs + (c.meta >> 8);
+  const int decision = __ldcg(&r->decision);
+  const float chi = __ldcg(&r->coef_hi), clo = __ldcg(&r->coef_lo);
+  if (!must_write(decision, chi, clo)) return;
+  chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
+}
+
+// ---------------------------------------------------------------------------
+// Single-launch variant (cooperative launch, so every block is resident).
+
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 5) k_clip_persistent(const NormArgs a, SyncWords* sync,
+                                                              long long timeout_ns) {
+  __shared__ FF red[kWarps];
+  __shared__ unsigned int s_gen0, s_claim;
+  __shared__ int s_flag, s_go;
+
+  // The generation before this call.  It is bumped only after every block
+  // has arrived, so each block reads the same value here.
+  if (threadIdx.x == 0) s_gen0 = *reinterpret_cast<volatile unsigned int*>(&sync->gen);
+
+  // Phase 1: the norm pass; the block that arrives last publishes the record.
+  const FF bsum = block_norm_pass(a, red);
+  const bool published = norm_arrive(a, bsum, red, &s_flag);
+
+  if (published) {
+    if (threadIdx.x == 0) {
+      sync->work = 0u;  // nobody claims before the generation moves
+      __threadfence();
+      atomicAdd(&sync->gen, 1u);  // release: the record was fenced above
+      s_go = 1;
+    }
+  } else if (threadIdx.x == 0) {
+    // Bounded wait for the record; on timeout flag it and write nothing.
+    const unsigned long long t0 = globaltimer();
+    int ok = 1;
+    while (ld_acquire(&sync->gen) == s_gen0) {
+      if (static_cast<long long>(globaltimer() - t0) > timeout_ns) {
+        atomicExch(&a.res->status, GCLIP_STATUS_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    s_go = ok;
+  }
+  __syncthreads();
+  if (!s_go) return;
+
+  const int decision = __ldcg(&a.res->decision);
+  const float chi = __ldcg(&a.res->coef_hi), clo = __ldcg(&a.res->coef_lo);
+  if (!must_write(decision, chi, clo)) return;
+  // Phase 2: chunks claimed one at a time from a shared counter, highest
+  // chunk first (most recently read).  Thread 0 claims the next chunk while
+  // the block scales the current one.
+  const uint64_t pol = policy_evict_first();
+  const unsigned int n = static_cast<unsigned int>(a.n_chunks);
+  if (threadIdx.x == 0) s_claim = atomicAdd(&sync->work, 1u);
+  __syncthreads();
+  unsigned int claim = s_claim;
+  while (claim < n) {
+    unsigned int next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(&sync->work, 1u);
+    chunk_scale<HintMem>(a.chunks[n - 1u - claim], chi, clo, pol);
+    __syncthreads();
+    if (threadIdx.x == 0) s_claim = next;
+    __syncthreads();
+    claim = s_claim;
+  }
+}
+
+}  // namespace gclip

@@ -1,0 +1,263 @@
+// reduce.cuh -- the arithmetic of the norm: per-thread sums of squares of a
+// chunk, the fixed block tree, the scaling of a chunk, the final reduction
+// with the decision in double, and the norm pass shared by both variants.
+// Included by gclip.cu only.
+#pragma once
+
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace gclip {
+
+// ---------------------------------------------------------------------------
+// Sum of squares of one chunk: this thread's share, in a fixed order.
+
+template <int DT, class M>
+__device__ __forceinline__ FF chunk_sumsq_thread(FF acc, uint64_t addr, uint32_t n, float s,
+                                                 uint64_t pol) {
+  const Span sp = make_span<DT>(addr, n);
+  const uint4* v = reinterpret_cast<const uint4*>(sp.body);
+  for (uint32_t base = threadIdx.x; base < sp.nvec; base += kUnroll * kThreads) {
+    uint4 buf[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t i = base + u * kThreads;
+      buf[u] = i < sp.nvec ? M::ld_norm(v + i, pol) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (base + u * kThreads < sp.nvec) acc = ff_add_f(acc, Fmt<DT>::sumsq(buf[u], s));
+    }
+  }
+  constexpr uint32_t B = Fmt<DT>::kBytes;
+  if (threadIdx.x < sp.head) {
+    const float y = __fmul_rn(Fmt<DT>::load1(addr + threadIdx.x * B), s);
+    acc = ff_add_f(acc, __fmul_rn(y, y));
+  }
+  if (threadIdx.x < sp.ntail) {
+    const float y =
+        __fmul_rn(Fmt<DT>::load1(addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B), s);
+    acc = ff_add_f(acc, __fmul_rn(y, y));
+  }
+  return acc;
+}
+
+// Fixed-shape tree over the block; the total is valid in thread 0.  `red`
+// holds kWarps entries; the trailing barrier lets the caller reuse it.
+__device__ __forceinline__ FF block_reduce(FF v, FF* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    FF o;
+    o.hi = __shfl_down_sync(0xffffffffu, v.hi, off);
+    o.lo = __shfl_down_sync(0xffffffffu, v.lo, off);
+    v = ff_add(v, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  FF r = {0.f, 0.f};
+  if (warp == 0) {
+    r = lane < kWarps ? red[lane] : FF{0.f, 0.f};
+#pragma unroll
+    for (int off = kWarps / 2; off > 0; off >>= 1) {
+      FF o;
+      o.hi = __shfl_down_sync(0xffffffffu, r.hi, off);
+      o.lo = __shfl_down_sync(0xffffffffu, r.lo, off);
+      r = ff_add(r, o);
+    }
+  }
+  __syncthreads();
+  return r;
+}
+
+// Add this thread's share of chunk `c` to its running accumulator.
+template <class M>
+__device__ __forceinline__ FF chunk_accumulate(FF acc, const clip_chunk_t& c, float s, uint64_t pol) {
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: return chunk_sumsq_thread<GCLIP_F32, M>(acc, c.addr, c.numel, s, pol);
+    case GCLIP_F16: return chunk_sumsq_thread<GCLIP_F16, M>(acc, c.addr, c.numel, s, pol);
+    default: return chunk_sumsq_thread<GCLIP_BF16, M>(acc, c.addr, c.numel, s, pol);
+  }
+}
+
+// The sum of squares of one chunk, valid in thread 0.
+template <class M>
+__device__ __forceinline__ FF chunk_sumsq(const clip_chunk_t& c, float s, FF* red, uint64_t pol) {
+  return block_reduce(chunk_accumulate<M>(FF{0.f, 0.f}, c, s, pol), red);
+}
+
+// ---------------------------------------------------------------------------
+// Scaling of one chunk in place.
+
+template <int DT, class M>
+__device__ __forceinline__ void chunk_scale_thread(uint64_t addr, uint32_t n, float chi, float clo,
+                                                   uint64_t pol) {
+  const Span sp = make_span<DT>(addr, n);
+  uint4* v = reinterpret_cast<uint4*>(sp.body);
+  for (uint32_t base = threadIdx.x; base < sp.nvec; base += kUnroll * kThreads) {
+    uint4 buf[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t i = base + u * kThreads;
+      buf[u] = i < sp.nvec ? M::ld_scale(v + i, pol) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t i = base + u * kThreads;
+      if (i < sp.nvec) M::st_scale(v + i, Fmt<DT>::scale(buf[u], chi, clo), pol);
+    }
+  }
+  constexpr uint32_t B = Fmt<DT>::kBytes;
+  if (threadIdx.x < sp.head) {
+    const uint64_t a = addr + threadIdx.x * B;
+    Fmt<DT>::store1(a, Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(a), chi, clo));
+  }
+  if (threadIdx.x < sp.ntail) {
+    const uint64_t a = addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B;
+    Fmt<DT>::store1(a, Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(a), chi, clo));
+  }
+}
+
+template <class M>
+__device__ __forceinline__ void chunk_scale(const clip_chunk_t& c, float chi, float clo, uint64_t pol) {
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: chunk_scale_thread<GCLIP_F32, M>(c.addr, c.numel, chi, clo, pol); break;
+    case GCLIP_F16: chunk_scale_thread<GCLIP_F16, M>(c.addr, c.numel, chi, clo, pol); break;
+    default: chunk_scale_thread<GCLIP_BF16, M>(c.addr, c.numel, chi, clo, pol); break;
+  }
+}
+
+__device__ __forceinline__ bool must_write(int decision, float chi, float clo) {
+  return decision != GCLIP_DECISION_SKIP && !(chi == 1.0f && clo == 0.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Final reduction over partial sums, square root and decision.  Runs on one
+// block of kThreads threads: thread t sums entries t, t + kThreads, ... in
+// increasing order, then the fixed block tree; thread 0 writes the record.
+//
+// The decision is taken in double from the float-float sum: S = hi + lo is
+// exact in double, norm = sqrt(S) and max_norm / norm are IEEE double
+// operations, and the multiplier inv_scale * max_norm / norm is handed to the
+// scaling pass as a float-float pair so that each output is rounded once.
+
+__device__ FF reduce_partials(const float2* partials, int64_t n, FF* red) {
+  FF acc = {0.f, 0.f};
+  int64_t c = threadIdx.x;
+  for (; c + 3 * kThreads < n; c += 4 * kThreads) {
+    const float2 p0 = __ldcg(partials + c);
+    const float2 p1 = __ldcg(partials + c + kThreads);
+    const float2 p2 = __ldcg(partials + c + 2 * kThreads);
+    const float2 p3 = __ldcg(partials + c + 3 * kThreads);
+    acc = ff_add(acc, FF{p0.x, p0.y});
+    acc = ff_add(acc, FF{p1.x, p1.y});
+    acc = ff_add(acc, FF{p2.x, p2.y});
+    acc = ff_add(acc, FF{p3.x, p3.y});
+  }
+  for (; c < n; c += kThreads) {
+    const float2 p = __ldcg(partials + c);
+    acc = ff_add(acc, FF{p.x, p.y});
+  }
+  return block_reduce(acc, red);
+}
+
+// The norm, flag, decision and multiplier from the float-float sum of
+// squares S = hi + lo (thread 0).
+__device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_result_t* res,
+                             float* out_norm, int32_t* out_flag) {
+  const double S = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
+  const bool nonfinite = !isfinite(acc.hi) || !isfinite(acc.lo) || S > static_cast<double>(FLT_MAX);
+  const double norm = sqrt(S);
+  int decision;
+  float chi = 1.0f, clo = 0.0f;
+  if (nonfinite) {
+    decision = GCLIP_DECISION_SKIP;
+  } else if (norm > static_cast<double>(max_norm)) {
+    decision = GCLIP_DECISION_CLIP;
+    const double k = static_cast<double>(inv_scale) * (static_cast<double>(max_norm) / norm);
+    chi = __double2float_rn(k);
+    clo = __double2float_rn(k - static_cast<double>(chi));
+  } else {
+    decision = GCLIP_DECISION_PASS;
+    chi = inv_scale;
+  }
+  const float norm_f = __double2float_rn(norm);
+  res->norm = norm_f;
+  res->nonfinite = nonfinite ? 1 : 0;
+  res->decision = decision;
+  res->coef_hi = chi;
+  res->coef_lo = clo;
+  res->sumsq_hi = acc.hi;
+  res->sumsq_lo = acc.lo;
+  res->calls = res->calls + 1u;
+  if (out_norm) *out_norm = norm_f;
+  if (out_flag) *out_flag = nonfinite ? 1 : 0;
+}
+
+__device__ void final_reduce(const float2* partials, int64_t n_chunks, float max_norm,
+                             float inv_scale, clip_result_t* res, float* out_norm,
+                             int32_t* out_flag, FF* red) {
+  const FF acc = reduce_partials(partials, n_chunks, red);
+  if (threadIdx.x == 0) decide_write(acc, max_norm, inv_scale, res, out_norm, out_flag);
+}
+
+// ---------------------------------------------------------------------------
+// The norm pass of the handle-based clip, shared by both variants.
+//
+// A grid of G blocks (G fixed per handle: the co-resident count of the
+// single-launch kernel, at most the number of chunks).  Block b takes chunks
+// b, b + G, b + 2G, ...; each of its threads keeps one float-float
+// accumulator over its share of all those chunks, in that order, and the
+// block tree combines the threads once at the end.  The block sum goes to
+// block_sums[b]; the block that arrives last reduces the G block sums in
+// fixed order (final_reduce) and publishes the record.  Which block arrives
+// last depends on timing; the arithmetic does not.
+
+struct NormArgs {
+  const clip_chunk_t* chunks;
+  int64_t n_chunks;
+  float2* block_sums;     // G entries
+  unsigned int* arrive;   // blocks done with the norm pass in this call
+  unsigned int expected;  // G, plus the test hook's extra arrivals
+  float max_norm;
+  float inv_scale;
+  clip_result_t* res;
+  float* out_norm;
+  int32_t* out_flag;
+  int64_t keep_from;      // chunks from here on are read with evict_last
+};
+
+__device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
+  const uint64_t pol_first = policy_evict_first();
+  const uint64_t pol_last = policy_evict_last();
+  FF acc = {0.f, 0.f};
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const clip_chunk_t ch = a.chunks[c];
+    acc = chunk_accumulate<HintMem>(acc, ch, a.inv_scale, c >= a.keep_from ? pol_last : pol_first);
+  }
+  return block_reduce(acc, red);
+}
+
+// Publish this block's sum; returns true (in every thread) in the block that
+// arrived last, after it has written the record.
+__device__ __forceinline__ bool norm_arrive(const NormArgs& a, FF bsum, FF* red, int* s_flag) {
+  if (threadIdx.x == 0) {
+    a.block_sums[blockIdx.x] = make_float2(bsum.hi, bsum.lo);
+    __threadfence();
+    const unsigned int t = atomicAdd(a.arrive, 1u);
+    *s_flag = (t + 1u == a.expected);
+  }
+  __syncthreads();
+  if (!*s_flag) return false;
+  __threadfence();
+  final_reduce(a.block_sums, gridDim.x, a.max_norm, a.inv_scale, a.res, a.out_norm, a.out_flag,
+               red);
+  if (threadIdx.x == 0) {
+    *a.arrive = 0u;  // every block has arrived: rearm for the next call
+    __threadfence();
+  }
+  return true;
+}
+
+}  // namespace gclip
