@@ -58,6 +58,8 @@ def parse_args(argv=None):
                    help="replay each run of clips as one captured CUDA graph")
     p.add_argument("--per-tensor", action="store_true",
                    help="clip each tensor by its own norm (clip_grad_norm_per_tensor)")
+    p.add_argument("--to-f32", action="store_true",
+                   help="clip out of place into fp32 buffers (clip_grad_norm_to_f32)")
     p.add_argument("--adamw", action="store_true",
                    help="time the fused clip + AdamW step instead of the clip alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -312,6 +314,9 @@ def run_gclip(args):
     P = 1 if args.warm else max(1, min(args.pool, args.steps))
     sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
     clippers = [g.GradClipper(s.tensors, variant=args.variant) for s in sets]
+    if args.to_f32:
+        for c, s_ in zip(clippers, sets):
+            c.attach_f32_out([torch.empty(t.numel(), device=dev) for t in s_.tensors])
     if args.l2_keep_mb is not None:
         for c in clippers:
             c.set_l2_keep(int(args.l2_keep_mb * (1 << 20)))
@@ -323,6 +328,8 @@ def run_gclip(args):
     def clip(c):
         if args.per_tensor:
             c.clip_per_tensor_(w.max_norm, w.inv_scale)
+        elif args.to_f32:
+            c.clip_to_f32_(w.max_norm, w.inv_scale)
         else:
             c.clip_(w.max_norm, w.inv_scale)
 
@@ -356,11 +363,15 @@ def run_gclip(args):
         writes = rec["decision"] != g.GCLIP_DECISION_SKIP and not (
             rec["coef_hi"] == 1.0 and rec["coef_lo"] == 0.0)
         written = w.numel if writes else 0
+        if args.to_f32:   # the gradients are only read; the outputs are always written
+            writes = False
+            written = w.numel if rec["decision"] != g.GCLIP_DECISION_SKIP else 0
     if args.warm and writes:
         print(json.dumps({"error": "--warm needs a workload whose clip writes nothing"}))
         return 2
     decision_name = {0: "pass", 1: "clip", 2: "skip"}[rec["decision"]]
-    nbytes = w.numel * w.elem_bytes + 2 * written * w.elem_bytes
+    nbytes = (w.numel * w.elem_bytes + written * (w.elem_bytes + 4) if args.to_f32
+              else w.numel * w.elem_bytes + 2 * written * w.elem_bytes)
 
     # warm-up
     restore()
@@ -443,8 +454,9 @@ def run_gclip(args):
         for k in range(3):
             seg[k].append(evs[k].elapsed_time(evs[k + 1]))
     seg_ms = [statistics.mean(s) for s in seg]
-    if args.per_tensor:
-        kernel, k_bytes, k_ms = "per-tensor clip (3 launches, timed region)", nbytes, per_step_ms
+    if args.per_tensor or args.to_f32:
+        kernel = "per-tensor clip (3 launches)" if args.per_tensor else "clip into fp32 (2 launches)"
+        k_bytes, k_ms = nbytes, per_step_ms
     elif args.variant.startswith("persistent"):
         kernel = "k_clip_persistent_tma" if args.variant.endswith("tma") else "k_clip_persistent"
         k_bytes, k_ms = nbytes, seg_ms[2]
@@ -475,7 +487,7 @@ def run_gclip(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e and not args.per_tensor:
+    if not args.no_e2e and not args.per_tensor and not args.to_f32:
         host = pristine.flat.cpu().pin_memory()
         norm_h = torch.empty(1, dtype=torch.float32).pin_memory()
         flag_h = torch.empty(1, dtype=torch.int32).pin_memory()
@@ -527,7 +539,8 @@ def run_gclip(args):
             "config": {
                 "workload": w.name, "description": w.description, "tensors": len(w.layout),
                 "elements": w.numel, "bytes_per_step": nbytes, "decision": decision_name,
-                "variant": "per_tensor" if args.per_tensor else args.variant, "pool": P,
+                "variant": ("per_tensor" if args.per_tensor else "to_f32" if args.to_f32
+                            else args.variant), "pool": P,
                 "l2_keep_mb": args.l2_keep_mb, "written_elements": written, "parallelism": f"replicas x{world}",
                 "l2": ("warm: one set re-read from L2, no flush" if args.warm else
                        "inputs larger than L2 (one set per step, pool of distinct sets); "
