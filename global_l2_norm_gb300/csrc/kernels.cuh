@@ -71,16 +71,12 @@ __device__ __forceinline__ void adamw1(float x, float& w, float& m, float& v, fl
   w = __fmaf_rn(-p.lr, upd, __fmul_rn(w, p.decay));
 }
 
-__device__ __forceinline__ void adamw4(const float (&x)[4], float4* w, float4* m, float4* v, float chi,
+__device__ __forceinline__ void adamw4(const float* x, float4& W, float4& M, float4& V, float chi,
                                        float clo, const AdamwArgs& p) {
-  float4 W = __ldcs(w), M = __ldcs(m), V = __ldcs(v);
   adamw1(x[0], W.x, M.x, V.x, chi, clo, p);
   adamw1(x[1], W.y, M.y, V.y, chi, clo, p);
   adamw1(x[2], W.z, M.z, V.z, chi, clo, p);
   adamw1(x[3], W.w, M.w, V.w, chi, clo, p);
-  __stcs(w, W);
-  __stcs(m, M);
-  __stcs(v, V);
 }
 
 template <int DT>
@@ -112,15 +108,30 @@ __device__ __forceinline__ void adamw_chunk(const clip_chunk_t& c, const TensorS
   const bool vec = ((reinterpret_cast<uint64_t>(w + sp.head) | reinterpret_cast<uint64_t>(m + sp.head) |
                      reinterpret_cast<uint64_t>(v + sp.head)) & 15u) == 0;
   if (vec) {
+    constexpr uint32_t Q = E / 4;  // float4s of state per gradient vector
     for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) {
-      float x[8];
-      widen_vec<DT>(HintMem::ld_scale(gv + i, pol), x);
+      // every load of this vector first, then the arithmetic, then the stores
+      const uint4 gvec = HintMem::ld_scale(gv + i, pol);
       const uint32_t k = sp.head + i * E;
+      float4* w4 = reinterpret_cast<float4*>(w + k);
+      float4* m4 = reinterpret_cast<float4*>(m + k);
+      float4* v4 = reinterpret_cast<float4*>(v + k);
+      float4 W[Q], M[Q], V[Q];
 #pragma unroll
-      for (uint32_t q = 0; q < E; q += 4) {
-        const float xs[4] = {x[q], x[q + 1], x[q + 2], x[q + 3]};
-        adamw4(xs, reinterpret_cast<float4*>(w + k + q), reinterpret_cast<float4*>(m + k + q),
-               reinterpret_cast<float4*>(v + k + q), chi, clo, p);
+      for (uint32_t q = 0; q < Q; ++q) {
+        W[q] = __ldcs(w4 + q);
+        M[q] = __ldcs(m4 + q);
+        V[q] = __ldcs(v4 + q);
+      }
+      float x[8];
+      widen_vec<DT>(gvec, x);
+#pragma unroll
+      for (uint32_t q = 0; q < Q; ++q) adamw4(x + 4 * q, W[q], M[q], V[q], chi, clo, p);
+#pragma unroll
+      for (uint32_t q = 0; q < Q; ++q) {
+        __stcs(w4 + q, W[q]);
+        __stcs(m4 + q, M[q]);
+        __stcs(v4 + q, V[q]);
       }
       if (p.zero_grads) HintMem::st_scale(gv + i, make_uint4(0, 0, 0, 0), pol);
     }
@@ -148,7 +159,7 @@ __device__ __forceinline__ void adamw_chunk(const clip_chunk_t& c, const TensorS
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_adamw(const clip_chunk_t* __restrict__ chunks,
+__global__ void __launch_bounds__(kThreads, 4) k_adamw(const clip_chunk_t* __restrict__ chunks,
                                                     int64_t n_chunks,
                                                     const TensorState* __restrict__ states,
                                                     const clip_result_t* res, const AdamwArgs p) {

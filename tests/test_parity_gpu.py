@@ -299,3 +299,29 @@ def test_barrier_timeout_reports_and_writes_nothing(variant):
         assert rec["decision"] == g.GCLIP_DECISION_CLIP
     rec["out_norm"], rec["out_flag"] = rec["norm"], rec["nonfinite"]
     compare(before, gs.tensors, rec, 1e-3, 1.0, "after-timeout")
+
+
+# -- CUDA graph capture ------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_captured_in_a_cuda_graph(variant):
+    """clip_grad_norm enqueues launches only (no sync, no allocation), so it
+    can be captured; replays of the graph clip the same buffers."""
+    gs = make_gradset("andrea14m", device=dev())
+    for t in gs.tensors:
+        t.mul_(40.0)                                   # the clip fires
+    pristine = clone_all(gs.tensors)
+    before = host_copies(gs.tensors)
+    with g.GradClipper(gs.tensors, variant=variant) as c:
+        c.clip_(1.0, 0.5)                              # first call outside capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            c.clip_(1.0, 0.5)
+        for _ in range(2):
+            restore(gs.tensors, pristine)
+            graph.replay()
+            torch.cuda.synchronize()
+            rec = c.result()
+            rec["out_norm"], rec["out_flag"] = float(c.norm.item()), int(c.flag.item())
+            compare(before, gs.tensors, rec, 1.0, 0.5, "graph")
