@@ -93,6 +93,9 @@ WORKLOADS = {
         "andrea120m", tuple(andrea_layout(768, 12)), 3e-5, "f32", 1.0, 1.0,
         spikes=1, spike_factor=50.0,
         description="ANDREA-120M fp32 grads, N(0,3e-5), one matrix x50, max_norm 1"),
+    "andrea120m_noclip": Workload(
+        "andrea120m_noclip", tuple(andrea_layout(768, 12)), 3e-5, "f32", 1.0, 1.0,
+        description="ANDREA-120M fp32 grads, N(0,3e-5), no spike, max_norm 1 (no clip)"),
     # 4 accumulated microbatches under loss scale 65536: the stored values are
     # the scaled sums, the clip unscales by 1/(65536*4) = 2^-18.
     "andrea120m_fp16": Workload(
