@@ -325,3 +325,23 @@ def test_captured_in_a_cuda_graph(variant):
             rec = c.result()
             rec["out_norm"], rec["out_flag"] = float(c.norm.item()), int(c.flag.item())
             compare(before, gs.tensors, rec, 1.0, 0.5, "graph")
+
+
+# -- accuracy of the norm -------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "andrea14m", "andrea120m", "andrea120m_fp16",
+                                  "andrea120m_bf16"])
+def test_norm_is_the_rounded_exact_norm(name):
+    """The float-float sum is good to ~2^-44, so the reported fp32 norm is the
+    oracle's (exact up to fp64 rounding) norm rounded to fp32 - at most one
+    ulp away in the rare case that the exact value sits next to a rounding
+    boundary.  A plain fp32 tree sum would drift several ulp at 92M terms."""
+    gs = make_gradset(name, device=dev())
+    before = host_copies(gs.tensors)
+    with g.GradClipper(gs.tensors) as c:
+        c.clip_(gs.max_norm, gs.inv_scale)
+        got = np.float32(c.result()["norm"])
+    _, r = oracle.default().clip(before, gs.max_norm, gs.inv_scale)
+    want = np.float32(r.norm)
+    ulps = abs(int(np.array([got]).view(np.int32)[0]) - int(np.array([want]).view(np.int32)[0]))
+    assert ulps <= 1, (float(got), float(want), ulps)
