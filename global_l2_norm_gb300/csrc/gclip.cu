@@ -249,7 +249,7 @@ int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
     void* a1[] = {&a};
     if (e == cudaSuccess)
       e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial),
-                     static_cast<unsigned int>(h->grid_persistent), s, a1, false);
+                     static_cast<unsigned int>(h->grid_persistent), s, a1, pdl);
     mark(1);
     mark(2);
     const clip_chunk_t* chunks = h->d_chunks;
@@ -486,7 +486,7 @@ int enqueue_norm_then(clip_handle_t h, float max_norm, float inv_scale, float* o
     gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag, 0);
     void* a1[] = {&a};
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial),
-                   static_cast<unsigned int>(h->grid_persistent), s, a1, false);
+                   static_cast<unsigned int>(h->grid_persistent), s, a1, true);
     if (e == cudaSuccess) e = launch_pdl(fn, static_cast<unsigned int>(nc), s, args, true);
   }
   if (e != cudaSuccess) {

@@ -16,6 +16,10 @@ __global__ void __launch_bounds__(kThreads) k_grad_norm_partial(const NormArgs a
   __shared__ int s_flag;
   // Let the dependent scaling launch be scheduled while this grid runs.
   asm volatile("griddepcontrol.launch_dependents;");
+  // Launched as a dependent of whatever the stream ran before (it may be the
+  // kernel that produced the gradients): wait for it to finish before
+  // reading any gradient.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const FF bsum = block_norm_pass(a, red);
   norm_arrive(a, bsum, red, &s_flag);
 }
@@ -39,6 +43,9 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __r
   const int decision = res->decision;
   const float chi = res->coef_hi, clo = res->coef_lo;
   if (!must_write(decision, chi, clo)) return;
+  // Real work follows: let the next dependent launch be scheduled now
+  // (blocks that write nothing trigger by exiting).
+  asm volatile("griddepcontrol.launch_dependents;");
   // Highest chunks first: the norm pass read them last and kept them in L2.
   const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
   chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
@@ -165,6 +172,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_adamw(const clip_chunk_t* __res
                                                     const clip_result_t* res, const AdamwArgs p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (__ldcg(&res->decision) == GCLIP_DECISION_SKIP) return;
+  // Real work follows: let the next dependent launch be scheduled now
+  // (blocks that write nothing trigger by exiting).
+  asm volatile("griddepcontrol.launch_dependents;");
   const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
   // Highest chunks first: the norm pass read their gradients last.
   const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
@@ -217,6 +227,9 @@ __global__ void __launch_bounds__(kThreads) k_to_f32(const clip_chunk_t* __restr
                                                      const clip_result_t* res) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (__ldcg(&res->decision) == GCLIP_DECISION_SKIP) return;
+  // Real work follows: let the next dependent launch be scheduled now
+  // (blocks that write nothing trigger by exiting).
+  asm volatile("griddepcontrol.launch_dependents;");
   const float chi = __ldcg(&res->coef_hi), clo = __ldcg(&res->coef_lo);
   const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
   const TensorState ts = outs[c.meta >> 8];
@@ -266,6 +279,9 @@ __global__ void __launch_bounds__(kThreads) k_scale_per_tensor(const clip_chunk_
   const int decision = __ldcg(&r->decision);
   const float chi = __ldcg(&r->coef_hi), clo = __ldcg(&r->coef_lo);
   if (!must_write(decision, chi, clo)) return;
+  // Real work follows: let the next dependent launch be scheduled now
+  // (blocks that write nothing trigger by exiting).
+  asm volatile("griddepcontrol.launch_dependents;");
   chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
 }
 
