@@ -100,6 +100,9 @@ class GradClipper:
         self._h = h
         self.norm = torch.zeros(1, dtype=torch.float32, device=self.device)
         self.flag = torch.zeros(1, dtype=torch.int32, device=self.device)
+        n = max(1, len(self.tensors))
+        self._pt_norms = torch.zeros(n, dtype=torch.float32, device=self.device)
+        self._pt_flags = torch.zeros(n, dtype=torch.int32, device=self.device)
         if variant is not None:
             self.set_variant(variant)
 
@@ -121,9 +124,6 @@ class GradClipper:
         """Clip every tensor by its own norm, in place.  Returns device tensors
         of the per-tensor norms (float32[n]) and nonfinite flags (int32[n])."""
         n = len(self.tensors)
-        if getattr(self, "_pt_norms", None) is None:
-            self._pt_norms = torch.zeros(max(1, n), dtype=torch.float32, device=self.device)
-            self._pt_flags = torch.zeros(max(1, n), dtype=torch.int32, device=self.device)
         check("clip_grad_norm_per_tensor", self._lib.clip_grad_norm_per_tensor(
             self._h, float(max_norm), float(inv_scale), self._pt_norms.data_ptr(),
             self._pt_flags.data_ptr(), _stream_handle(stream, self.device)))
