@@ -395,6 +395,55 @@ int oracle_clip_sample(const oracle_tensor *in, int32_t n_tensors,
     return 0;
 }
 
+/* Gradient accumulation, the last microbatch: every element of acc[t]
+ * becomes acc + add, the sum of the two stored values rounded once to nearest
+ * even in the tensor's own format.  "Grow a language model: backprop"
+ * (unhomeschool.com, Vietnamese), section "Accumulation across
+ * microbatches": the backward kernels add their contribution into the
+ * gradient buffer (+=), which holds the running sum until zero_grads.  The
+ * sum is formed in double and rounded once; double carries more than twice
+ * the significand bits of each format plus two, so this is the correctly
+ * rounded sum of the format.  Returns 0, or -1 for mismatched descriptors. */
+int oracle_accumulate(const oracle_tensor *acc, const oracle_tensor *add, int32_t n_tensors)
+{
+    for (int32_t t = 0; t < n_tensors; ++t)
+        if (acc[t].numel != add[t].numel || acc[t].dtype != add[t].dtype ||
+            acc[t].numel < 0 || !check_dtype(acc[t].dtype))
+            return -1;
+    for (int32_t t = 0; t < n_tensors; ++t) {
+        int32_t dt = acc[t].dtype;
+        for (int64_t i = 0; i < acc[t].numel; ++i) {
+            double a = oracle_decode(acc[t].data, i, dt);
+            double b = oracle_decode(add[t].data, i, dt);
+#if ORACLE_MUTANT == 16
+            double v = a - b;                  /* mistake: addend subtracted */
+#else
+            double v = a + b;
+#endif
+            oracle_encode((void *)acc[t].data, i, dt, v);
+        }
+    }
+    return 0;
+}
+
+/* The last microbatch's accumulation followed by the clip of the whole
+ * buffer, in that order (the glossary page, "Order changes the result": with
+ * accumulation the clip acts on the whole effective batch).  acc[t] is
+ * rewritten in place: first with the rounded sums, then, on PASS or CLIP,
+ * with the clipped values.  On SKIP the sums stay (the accumulation is not
+ * part of the stopped update).  Returns 0, or -1 for bad arguments. */
+int oracle_clip_accumulate(const oracle_tensor *acc, const oracle_tensor *add,
+                           int32_t n_tensors, double max_norm, double inv_scale,
+                           oracle_result *res)
+{
+    if (!(max_norm > 0.0) || !isfinite(max_norm) || !(inv_scale > 0.0) ||
+        !isfinite(inv_scale) || n_tensors < 0)
+        return -1;
+    if (oracle_accumulate(acc, add, n_tensors) != 0)
+        return -1;
+    return oracle_clip(acc, acc, n_tensors, max_norm, inv_scale, res);
+}
+
 /* Out-of-place clip into fp32 buffers: the same decision as oracle_clip, and
  * every element x becomes round_fp32(x * inv_scale * coef) in out[t] (fp32
  * host arrays of the tensors' numel); on SKIP the outputs are not written.
