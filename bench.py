@@ -58,6 +58,8 @@ def parse_args(argv=None):
                    help="replay each run of clips as one captured CUDA graph")
     p.add_argument("--per-tensor", action="store_true",
                    help="clip each tensor by its own norm (clip_grad_norm_per_tensor)")
+    p.add_argument("--accumulate", action="store_true",
+                   help="add the last microbatch's gradients, then clip (clip_grad_norm_accumulate)")
     p.add_argument("--to-f32", action="store_true",
                    help="clip out of place into fp32 buffers (clip_grad_norm_to_f32)")
     p.add_argument("--adamw", action="store_true",
@@ -301,6 +303,9 @@ def run_gclip(args):
     if world != args.gpus:
         print(json.dumps({"error": f"--gpus {args.gpus} but WORLD_SIZE={world}"}))
         return 2
+    if args.per_tensor + args.to_f32 + args.accumulate > 1:
+        print(json.dumps({"error": "--per-tensor, --to-f32 and --accumulate exclude one another"}))
+        return 2
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -317,6 +322,11 @@ def run_gclip(args):
     if args.to_f32:
         for c, s_ in zip(clippers, sets):
             c.attach_f32_out([torch.empty(t.numel(), device=dev) for t in s_.tensors])
+    addends = []
+    if args.accumulate:   # the last microbatch's gradients: another seeded set per pool entry
+        addends = [make_gradset(w, seed=4321, device=dev, flat=True) for _ in range(P)]
+        for c, a_ in zip(clippers, addends):
+            c.attach_addend(a_.tensors)
     if args.l2_keep_mb is not None:
         for c in clippers:
             c.set_l2_keep(int(args.l2_keep_mb * (1 << 20)))
@@ -330,6 +340,8 @@ def run_gclip(args):
             c.clip_per_tensor_(w.max_norm, w.inv_scale)
         elif args.to_f32:
             c.clip_to_f32_(w.max_norm, w.inv_scale)
+        elif args.accumulate:
+            c.clip_accumulate_(w.max_norm, w.inv_scale)
         else:
             c.clip_(w.max_norm, w.inv_scale)
 
@@ -354,8 +366,12 @@ def run_gclip(args):
         rec = {"decision": g.GCLIP_DECISION_CLIP if writes else g.GCLIP_DECISION_PASS}
     else:
         rec = clippers[0].result()
-        ref_norm = math.sqrt(sum(float(t.double().square().sum()) for t in pristine.tensors)
+        ref_sets = pristine.tensors
+        if args.accumulate:   # the sums, each rounded by torch's own addition in the format
+            ref_sets = [a + b for a, b in zip(pristine.tensors, addends[0].tensors)]
+        ref_norm = math.sqrt(sum(float(t.double().square().sum()) for t in ref_sets)
                              ) * w.inv_scale
+        del ref_sets
         if math.isfinite(ref_norm):
             assert abs(rec["norm"] - ref_norm) <= 1e-5 * ref_norm, (rec["norm"], ref_norm)
         else:
@@ -366,12 +382,17 @@ def run_gclip(args):
         if args.to_f32:   # the gradients are only read; the outputs are always written
             writes = False
             written = w.numel if rec["decision"] != g.GCLIP_DECISION_SKIP else 0
+        scaled = written
+        if args.accumulate:   # the norm pass always writes the sums
+            writes = True
     if args.warm and writes:
         print(json.dumps({"error": "--warm needs a workload whose clip writes nothing"}))
         return 2
     decision_name = {0: "pass", 1: "clip", 2: "skip"}[rec["decision"]]
     nbytes = (w.numel * w.elem_bytes + written * (w.elem_bytes + 4) if args.to_f32
               else w.numel * w.elem_bytes + 2 * written * w.elem_bytes)
+    if args.accumulate:   # read x and a, write x + a; then the scaling pass if it writes
+        nbytes = 3 * w.numel * w.elem_bytes + 2 * scaled * w.elem_bytes
 
     # warm-up
     restore()
@@ -437,7 +458,7 @@ def run_gclip(args):
 
     # per-kernel durations for the roofline (events between the launches)
     launches_per_step = 3 if args.per_tensor else (
-        1 if args.variant.startswith("persistent") else 2)
+        2 if args.to_f32 or args.accumulate or not args.variant.startswith("persistent") else 1)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in evs:           # torch creates the CUDA event on its first record
         e.record(stream)
@@ -454,8 +475,10 @@ def run_gclip(args):
         for k in range(3):
             seg[k].append(evs[k].elapsed_time(evs[k + 1]))
     seg_ms = [statistics.mean(s) for s in seg]
-    if args.per_tensor or args.to_f32:
-        kernel = "per-tensor clip (3 launches)" if args.per_tensor else "clip into fp32 (2 launches)"
+    if args.per_tensor or args.to_f32 or args.accumulate:
+        kernel = ("per-tensor clip (3 launches)" if args.per_tensor else
+                  "clip into fp32 (2 launches)" if args.to_f32 else
+                  "accumulate + clip (2 launches)")
         k_bytes, k_ms = nbytes, per_step_ms
     elif args.variant.startswith("persistent"):
         kernel = "k_clip_persistent_tma" if args.variant.endswith("tma") else "k_clip_persistent"
@@ -487,7 +510,7 @@ def run_gclip(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e and not args.per_tensor and not args.to_f32:
+    if not args.no_e2e and not args.per_tensor and not args.to_f32 and not args.accumulate:
         host = pristine.flat.cpu().pin_memory()
         norm_h = torch.empty(1, dtype=torch.float32).pin_memory()
         flag_h = torch.empty(1, dtype=torch.int32).pin_memory()
@@ -540,6 +563,7 @@ def run_gclip(args):
                 "workload": w.name, "description": w.description, "tensors": len(w.layout),
                 "elements": w.numel, "bytes_per_step": nbytes, "decision": decision_name,
                 "variant": ("per_tensor" if args.per_tensor else "to_f32" if args.to_f32
+                            else "accumulate" if args.accumulate
                             else args.variant), "pool": P,
                 "l2_keep_mb": args.l2_keep_mb, "written_elements": written, "parallelism": f"replicas x{world}",
                 "l2": ("warm: one set re-read from L2, no flush" if args.warm else

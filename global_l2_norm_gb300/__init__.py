@@ -158,6 +158,29 @@ class GradClipper:
             self.flag.data_ptr(), _stream_handle(stream, self.device)))
         return self.norm, self.flag
 
+    # -- the last microbatch's accumulation folded into the clip -------------
+    def attach_addend(self, addends) -> None:
+        """Attach CUDA tensors, one per gradient tensor (same numel and dtype),
+        that clip_accumulate_ adds into the gradients.  They stay owned by the
+        caller and are only read."""
+        addends = list(addends)
+        arr = (ctypes.c_void_p * max(1, len(addends)))()
+        for i, (a, g) in enumerate(zip(addends, self.tensors)):
+            if a.dtype != g.dtype or not a.is_contiguous() or a.device != self.device:
+                raise ValueError("addends must be contiguous, of the gradient's dtype and device")
+            arr[i] = a.data_ptr() if a.numel() else None
+        self._addends = addends
+        check("clip_attach_addend", self._lib.clip_attach_addend(self._h, arr, len(addends)))
+
+    def clip_accumulate_(self, max_norm: float, inv_scale: float = 1.0, stream=None):
+        """Add the attached addends into the gradients, then clip the sums in
+        place (see clip_grad_norm_accumulate in include/gclip.h).  Returns
+        (norm, flag) device tensors."""
+        check("clip_grad_norm_accumulate", self._lib.clip_grad_norm_accumulate(
+            self._h, float(max_norm), float(inv_scale), self.norm.data_ptr(),
+            self.flag.data_ptr(), _stream_handle(stream, self.device)))
+        return self.norm, self.flag
+
     # -- fused clip + AdamW --------------------------------------------------
     def attach_adamw(self, states) -> None:
         """Attach fp32 (w, m, v) CUDA tensors, one triple per gradient tensor

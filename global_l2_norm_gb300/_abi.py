@@ -95,6 +95,8 @@ _SIGNATURES = {
     "clip_grad_norm_per_tensor": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float, _P, _P, _P]),
     "clip_read_per_tensor": (ctypes.c_int, [_P, ctypes.POINTER(clip_result_t), ctypes.c_int32, _P]),
     "clip_grad_norm_to_f32": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float, _P, _P, _P]),
+    "clip_attach_addend": (ctypes.c_int, [_P, ctypes.POINTER(_P), ctypes.c_int32]),
+    "clip_grad_norm_accumulate": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float, _P, _P, _P]),
     "clip_grad_norm_adamw": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float,
                                             ctypes.POINTER(clip_adamw_params_t), ctypes.c_int64,
                                             _P, _P, _P]),

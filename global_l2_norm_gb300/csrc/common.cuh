@@ -103,6 +103,15 @@ struct Fmt<GCLIP_F32> {
   __device__ static __forceinline__ float scale1(float x, float chi, float clo) {
     return __fmaf_rn(x, chi, __fmul_rn(x, clo));
   }
+  // Element-wise x + a of two stored vectors, each sum rounded once.
+  __device__ static __forceinline__ uint4 add(uint4 x, uint4 a) {
+    return make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(x.x), __uint_as_float(a.x))),
+                      __float_as_uint(__fadd_rn(__uint_as_float(x.y), __uint_as_float(a.y))),
+                      __float_as_uint(__fadd_rn(__uint_as_float(x.z), __uint_as_float(a.z))),
+                      __float_as_uint(__fadd_rn(__uint_as_float(x.w), __uint_as_float(a.w))));
+  }
+  // A float rounded to the storage format (here: itself).
+  __device__ static __forceinline__ float round1(float v) { return v; }
 };
 
 template <>
@@ -146,6 +155,20 @@ struct Fmt<GCLIP_F16> {
     return make_uint4(scale_word(v.x, chi, clo), scale_word(v.y, chi, clo),
                       scale_word(v.z, chi, clo), scale_word(v.w, chi, clo));
   }
+  // Element-wise x + a, each sum rounded once to the format: the float sum
+  // of two values of a format with p <= 11 significand bits, rounded again
+  // to the format, is the correctly rounded sum (24 >= 2p + 2).
+  __device__ static __forceinline__ uint32_t add_word(uint32_t x, uint32_t a) {
+    const float2 f = widen(x), g = widen(a);
+    return narrow(__fadd_rn(f.x, g.x), __fadd_rn(f.y, g.y));
+  }
+  __device__ static __forceinline__ uint4 add(uint4 x, uint4 a) {
+    return make_uint4(add_word(x.x, a.x), add_word(x.y, a.y), add_word(x.z, a.z),
+                      add_word(x.w, a.w));
+  }
+  __device__ static __forceinline__ float round1(float v) {
+    return __half2float(__float2half_rn(v));
+  }
 };
 
 template <>
@@ -187,6 +210,20 @@ struct Fmt<GCLIP_BF16> {
   __device__ static __forceinline__ uint4 scale(uint4 v, float chi, float clo) {
     return make_uint4(scale_word(v.x, chi, clo), scale_word(v.y, chi, clo),
                       scale_word(v.z, chi, clo), scale_word(v.w, chi, clo));
+  }
+  // Element-wise x + a, each sum rounded once to the format: the float sum
+  // of two values of a format with p <= 11 significand bits, rounded again
+  // to the format, is the correctly rounded sum (24 >= 2p + 2).
+  __device__ static __forceinline__ uint32_t add_word(uint32_t x, uint32_t a) {
+    const float2 f = widen(x), g = widen(a);
+    return narrow(__fadd_rn(f.x, g.x), __fadd_rn(f.y, g.y));
+  }
+  __device__ static __forceinline__ uint4 add(uint4 x, uint4 a) {
+    return make_uint4(add_word(x.x, a.x), add_word(x.y, a.y), add_word(x.z, a.z),
+                      add_word(x.w, a.w));
+  }
+  __device__ static __forceinline__ float round1(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
   }
 };
 

@@ -66,6 +66,7 @@ struct gclip_handle {
   std::vector<clip_tensor_desc_t> descs;   // the gradient tensors, as created
   gclip::TensorState* d_states;            // AdamW state table (NULL until attached)
   gclip::TensorState* d_outs;              // fp32 output table (NULL until attached)
+  gclip::TensorState* d_adds;              // addend table (NULL until attached)
 };
 
 namespace {
@@ -348,6 +349,7 @@ extern "C" int clip_destroy(clip_handle_t h) {
     if (cudaFree(h->arena) != cudaSuccess) rc = GCLIP_ERR_CUDA;
     if (h->d_states != nullptr && cudaFree(h->d_states) != cudaSuccess) rc = GCLIP_ERR_CUDA;
     if (h->d_outs != nullptr && cudaFree(h->d_outs) != cudaSuccess) rc = GCLIP_ERR_CUDA;
+    if (h->d_adds != nullptr && cudaFree(h->d_adds) != cudaSuccess) rc = GCLIP_ERR_CUDA;
     cudaGetLastError();
   }
   delete h;
@@ -422,11 +424,12 @@ extern "C" int clip_debug_barrier(clip_handle_t h, int32_t extra_arrivals, int64
 
 namespace {
 
-// Validate per-tensor fp32 arrays (`per` of them for each tensor, `ptrs`
-// laid out tensor by tensor) against the handle's gradients, and replace
-// *slot with a device table of {gradient base, arrays...}.
-int attach_table(clip_handle_t h, const float* const* ptrs, int per, int32_t n_tensors,
-                 gclip::TensorState** slot) {
+// Validate per-tensor arrays (`per` of them for each tensor, `ptrs` laid out
+// tensor by tensor; fp32, or of the gradient's own format with grad_dtype)
+// against the handle's gradients, and replace *slot with a device table of
+// {gradient base, arrays...}.
+int attach_table(clip_handle_t h, const void* const* ptrs, int per, int32_t n_tensors,
+                 gclip::TensorState** slot, bool grad_dtype = false) {
   if (h == nullptr || n_tensors != static_cast<int32_t>(h->descs.size()) ||
       (n_tensors > 0 && ptrs == nullptr))
     return GCLIP_ERR_INVALID_ARG;
@@ -438,10 +441,10 @@ int attach_table(clip_handle_t h, const float* const* ptrs, int per, int32_t n_t
     table[t].g = reinterpret_cast<uint64_t>(d.ptr);
     table[t].w = table[t].m = table[t].v = 0;
     for (int k = 0; k < per; ++k) {
-      const float* a = ptrs[static_cast<size_t>(t) * per + k];
+      const void* a = ptrs[static_cast<size_t>(t) * per + k];
       f[k] = reinterpret_cast<uint64_t>(a);
       if (d.numel == 0) continue;
-      clip_tensor_desc_t s = {const_cast<float*>(a), d.numel, GCLIP_F32, 0};
+      clip_tensor_desc_t s = {const_cast<void*>(a), d.numel, grad_dtype ? d.dtype : GCLIP_F32, 0};
       all.push_back(s);
     }
   }
@@ -507,12 +510,55 @@ extern "C" int clip_attach_adamw(clip_handle_t h, const clip_adamw_state_t* stat
     ptrs.push_back(states[t].m);
     ptrs.push_back(states[t].v);
   }
-  return attach_table(h, ptrs.data(), 3, n_tensors, &h->d_states);
+  return attach_table(h, reinterpret_cast<const void* const*>(ptrs.data()), 3, n_tensors,
+                      &h->d_states);
 }
 
 extern "C" int clip_attach_f32_out(clip_handle_t h, float* const* outs, int32_t n_tensors) {
   if (h == nullptr) return GCLIP_ERR_INVALID_ARG;
-  return attach_table(h, const_cast<const float* const*>(outs), 1, n_tensors, &h->d_outs);
+  return attach_table(h, const_cast<const void* const*>(reinterpret_cast<void* const*>(outs)), 1,
+                      n_tensors, &h->d_outs);
+}
+
+extern "C" int clip_attach_addend(clip_handle_t h, const void* const* addends, int32_t n_tensors) {
+  if (h == nullptr) return GCLIP_ERR_INVALID_ARG;
+  return attach_table(h, addends, 1, n_tensors, &h->d_adds, true);
+}
+
+extern "C" int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float inv_scale,
+                                         float* out_norm, int32_t* out_nonfinite_flag,
+                                         void* stream) {
+  if (h == nullptr || h->d_adds == nullptr || !valid_scalar(max_norm) || !valid_scalar(inv_scale))
+    return GCLIP_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t nc = h->n_chunks;
+  cudaError_t e = cudaSuccess;
+  if (nc == 0) {
+    const float2* partials = h->d_partials;
+    void* a[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm,
+                 &out_nonfinite_flag};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a, false);
+  } else {
+    gclip::NormArgs a =
+        norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_nonfinite_flag, 0);
+    const gclip::TensorState* adds = h->d_adds;
+    void* a1[] = {&a, &adds};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_accumulate),
+                   static_cast<unsigned int>(h->grid_persistent), s, a1, true);
+    const clip_chunk_t* chunks = h->d_chunks;
+    const clip_result_t* cres = h->d_result;
+    void* a2[] = {&chunks, &nc, &cres};
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale),
+                     static_cast<unsigned int>(nc), s, a2, true);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  return GCLIP_OK;
 }
 
 extern "C" int clip_grad_norm_to_f32(clip_handle_t h, float max_norm, float inv_scale,

@@ -241,6 +241,34 @@ __global__ void __launch_bounds__(kThreads) k_to_f32(const clip_chunk_t* __restr
 }
 
 // ---------------------------------------------------------------------------
+// Accumulation epilogue: the norm pass of the split variant with the last
+// microbatch's gradients added in (x <- x + a, stored back, then squared).
+// The same G blocks take the same chunks in the same order as
+// k_grad_norm_partial, so the norm, the decision and the scaling that
+// k_grad_scale then applies are bit for bit those of a separate += followed
+// by the clip.  `adds[t]` holds tensor t's gradient base (g) and its addend
+// base (w); an addend element sits at the same element offset as its
+// gradient element.
+
+__global__ void __launch_bounds__(kThreads, 5) k_grad_norm_accumulate(const NormArgs a,
+                                                                     const TensorState* __restrict__ adds) {
+  __shared__ FF red[kWarps];
+  __shared__ int s_flag;
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t pol_first = policy_evict_first();
+  const uint64_t pol_last = policy_evict_last();
+  FF acc = {0.f, 0.f};
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const clip_chunk_t ch = a.chunks[c];
+    const TensorState ts = adds[ch.meta >> 8];
+    acc = chunk_add_accumulate(acc, ch, ts.w + (ch.addr - ts.g), a.inv_scale,
+                               c >= a.keep_from ? pol_last : pol_first);
+  }
+  norm_arrive(a, block_reduce(acc, red), red, &s_flag);
+}
+
+// ---------------------------------------------------------------------------
 // Per-tensor clipping: each tensor clipped by its own norm.  One block per
 // chunk writes the chunk's sum of squares; one block per tensor reduces its
 // chunks' sums (the same fixed order as the final reduction) and decides;

@@ -88,6 +88,95 @@ __device__ __forceinline__ FF chunk_sumsq(const clip_chunk_t& c, float s, FF* re
 }
 
 // ---------------------------------------------------------------------------
+// The last microbatch's accumulation fused into the norm pass: every element
+// of a chunk becomes x + a (a from the addend tensor at the same offset),
+// rounded once to the format and stored back, and its square joins this
+// thread's accumulator in the order chunk_sumsq_thread uses (vectors
+// threadIdx.x, threadIdx.x + kThreads, ..., then the head element, then the
+// tail element), so the norm equals that of a separate += followed by the
+// clip.  An addend whose offset within 16 bytes differs from its gradient's
+// is read element by element; the order of the arithmetic is the same.
+
+constexpr int kAddUnroll = 2;  // vector pairs in flight per thread
+
+// 16 bytes of elements from an address aligned only to the element size.
+template <int DT>
+__device__ __forceinline__ uint4 load_vec_elems(uint64_t a) {
+  if constexpr (Fmt<DT>::kBytes == 4) {
+    const unsigned int* p = reinterpret_cast<const unsigned int*>(a);
+    return make_uint4(__ldcs(p), __ldcs(p + 1), __ldcs(p + 2), __ldcs(p + 3));
+  } else {
+    const unsigned short* p = reinterpret_cast<const unsigned short*>(a);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = static_cast<uint32_t>(__ldcs(p + 2 * k)) |
+             (static_cast<uint32_t>(__ldcs(p + 2 * k + 1)) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// One scalar element: x + a rounded to the format, stored, squared.
+template <int DT>
+__device__ __forceinline__ FF add_sumsq1(FF acc, uint64_t x_at, uint64_t a_at, float s) {
+  const float r = Fmt<DT>::round1(__fadd_rn(Fmt<DT>::load1(x_at), Fmt<DT>::load1(a_at)));
+  Fmt<DT>::store1(x_at, r);
+  const float y = __fmul_rn(r, s);
+  return ff_add_f(acc, __fmul_rn(y, y));
+}
+
+template <int DT>
+__device__ __forceinline__ FF chunk_add_sumsq_thread(FF acc, uint64_t addr, uint64_t add_addr,
+                                                     uint32_t n, float s, uint64_t pol) {
+  constexpr uint32_t B = Fmt<DT>::kBytes;
+  const Span sp = make_span<DT>(addr, n);
+  uint4* v = reinterpret_cast<uint4*>(sp.body);
+  const uint64_t add_body = add_addr + static_cast<uint64_t>(sp.head) * B;
+  const bool aligned = (add_body & 15u) == 0;  // the same in every thread
+  const uint4* av = reinterpret_cast<const uint4*>(add_body);
+  const uint64_t pol_add = policy_evict_first();  // the addend is read once
+  for (uint32_t base = threadIdx.x; base < sp.nvec; base += kAddUnroll * kThreads) {
+    uint4 x[kAddUnroll], a[kAddUnroll];
+#pragma unroll
+    for (int u = 0; u < kAddUnroll; ++u) {
+      const uint32_t i = base + u * kThreads;
+      x[u] = make_uint4(0, 0, 0, 0);
+      a[u] = make_uint4(0, 0, 0, 0);
+      if (i < sp.nvec) {
+        x[u] = HintMem::ld(v + i, pol);
+        a[u] = aligned ? HintMem::ld(av + i, pol_add)
+                       : load_vec_elems<DT>(add_body + static_cast<uint64_t>(i) * 16u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAddUnroll; ++u) {
+      const uint32_t i = base + u * kThreads;
+      if (i < sp.nvec) {
+        const uint4 sum = Fmt<DT>::add(x[u], a[u]);
+        HintMem::st_scale(v + i, sum, pol);
+        acc = ff_add_f(acc, Fmt<DT>::sumsq(sum, s));
+      }
+    }
+  }
+  if (threadIdx.x < sp.head)
+    acc = add_sumsq1<DT>(acc, addr + threadIdx.x * B, add_addr + threadIdx.x * B, s);
+  if (threadIdx.x < sp.ntail) {
+    const uint64_t off = static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B;
+    acc = add_sumsq1<DT>(acc, addr + off, add_addr + off, s);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ FF chunk_add_accumulate(FF acc, const clip_chunk_t& c, uint64_t add_addr,
+                                                   float s, uint64_t pol) {
+  switch (c.meta & 0xffu) {
+    case GCLIP_F32: return chunk_add_sumsq_thread<GCLIP_F32>(acc, c.addr, add_addr, c.numel, s, pol);
+    case GCLIP_F16: return chunk_add_sumsq_thread<GCLIP_F16>(acc, c.addr, add_addr, c.numel, s, pol);
+    default: return chunk_add_sumsq_thread<GCLIP_BF16>(acc, c.addr, add_addr, c.numel, s, pol);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Scaling of one chunk in place.
 
 template <int DT, class M>

@@ -386,6 +386,43 @@ int clip_grad_norm_to_f32(clip_handle_t h, float max_norm, float inv_scale,
                           float *out_norm, int32_t *out_nonfinite_flag,
                           void *stream);
 
+/* ------------------------------------------------------------------------
+ * Accumulation epilogue.  "Grow a language model: backprop" (unhomeschool.com,
+ * Vietnamese), section "Accumulation across microbatches": with several
+ * microbatches per step the backward kernels add (+=) into the gradient
+ * buffers, which hold the running sum; the glossary page, section "Order
+ * changes the result", clips only after the whole effective batch is in.
+ * These two calls fold the last microbatch's += into the clip's norm pass:
+ * the pass that reads the gradients to square them also adds the addend and
+ * writes the sum back, so the sum costs no read of its own. */
+
+/* clip_attach_addend -- addends[i] is added into descriptor i's gradient by
+ * clip_grad_norm_accumulate: a device array of the same numel and format
+ * (dtype), aligned to the element size (the same offset within 16 bytes as
+ * its gradient lets the kernel use vector loads), not overlapping any
+ * gradient or other addend.  Empty tensors may have NULL.  The arrays stay
+ * owned by the caller and are only read.  Copies a table of pointers to the
+ * device (the only allocation); a new call replaces the table.  Returns
+ * GCLIP_OK, GCLIP_ERR_INVALID_ARG (NULL handle, count different from the
+ * handle's tensors, NULL, misaligned or overlapping arrays), GCLIP_ERR_OOM
+ * or GCLIP_ERR_CUDA. */
+int clip_attach_addend(clip_handle_t h, const void *const *addends, int32_t n_tensors);
+
+/* clip_grad_norm_accumulate -- every gradient element x becomes x + a (its
+ * addend element), the sum rounded once to nearest even in the gradient's
+ * format and stored in place; then the clip of clip_grad_norm on the sums:
+ * the same norm, flag, decision and outputs, bit for bit, as adding the
+ * addends with the format's own addition and then calling clip_grad_norm
+ * with the split variant.  The sums are stored whatever the decision: on
+ * SKIP (a nonfinite sum) the gradients hold the unscaled, unclipped sums.
+ * Two launches (the norm pass with the addition, then the scaling),
+ * whatever clip_set_variant chose; asynchronous, no allocation.  Returns
+ * GCLIP_OK; GCLIP_ERR_INVALID_ARG (NULL handle, no addends attached, bad
+ * max_norm / inv_scale); GCLIP_ERR_CUDA. */
+int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float inv_scale,
+                              float *out_norm, int32_t *out_nonfinite_flag,
+                              void *stream);
+
 /* clip_grad_norm_flat_noalloc -- the same clip for one contiguous gradient
  * buffer, for callers that cannot allocate device memory.
  *

@@ -129,6 +129,11 @@ class Oracle:
                                          ctypes.c_int32, ctypes.c_double, ctypes.c_double,
                                          ctypes.POINTER(_Result)]
         L.oracle_clip_to_f32.restype = ctypes.c_int
+        L.oracle_accumulate.argtypes = [ctypes.POINTER(_Tensor), ctypes.POINTER(_Tensor),
+                                        ctypes.c_int32]
+        L.oracle_accumulate.restype = ctypes.c_int
+        L.oracle_clip_accumulate.argtypes = L.oracle_clip.argtypes
+        L.oracle_clip_accumulate.restype = ctypes.c_int
         L.oracle_sumsq.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int32,
                                    ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_int32)]
@@ -182,6 +187,32 @@ class Oracle:
             raise ValueError("oracle_clip_sample rejected its arguments")
         return slots, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
                                    res.decision)
+
+    def accumulate(self, tensors, addends):
+        """Return copies of `tensors` with `addends` added element by element,
+        each sum rounded once to its format; the inputs are not modified."""
+        outs = [OracleTensor(t.data.copy(), t.dtype) for t in tensors]
+        if len(addends) != len(tensors):
+            raise ValueError("one addend per tensor")
+        rc = self._lib.oracle_accumulate(self._descs(outs), self._descs(addends), len(outs))
+        if rc != 0:
+            raise ValueError("oracle_accumulate rejected its arguments")
+        return outs
+
+    def clip_accumulate(self, tensors, addends, max_norm: float, inv_scale: float = 1.0):
+        """The last microbatch's accumulation, then the clip of the sums:
+        returns (new copies of `tensors`, OracleResult); inputs unmodified."""
+        outs = [OracleTensor(t.data.copy(), t.dtype) for t in tensors]
+        if len(addends) != len(tensors):
+            raise ValueError("one addend per tensor")
+        res = _Result()
+        rc = self._lib.oracle_clip_accumulate(self._descs(outs), self._descs(addends), len(outs),
+                                              float(max_norm), float(inv_scale),
+                                              ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_clip_accumulate rejected its arguments")
+        return outs, OracleResult(res.sumsq, res.norm, res.coef, bool(res.nonfinite),
+                                  res.decision)
 
     def clip_to_f32(self, tensors, max_norm: float, inv_scale: float = 1.0, fill=np.nan):
         """Out-of-place clip into new float32 arrays (left at `fill` on

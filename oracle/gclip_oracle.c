@@ -439,9 +439,16 @@ int oracle_clip_accumulate(const oracle_tensor *acc, const oracle_tensor *add,
     if (!(max_norm > 0.0) || !isfinite(max_norm) || !(inv_scale > 0.0) ||
         !isfinite(inv_scale) || n_tensors < 0)
         return -1;
+#if ORACLE_MUTANT == 17
+    /* mistake: each contribution clipped before it is added */
+    if (oracle_clip(acc, acc, n_tensors, max_norm, inv_scale, res) != 0)
+        return -1;
+    return oracle_accumulate(acc, add, n_tensors);
+#else
     if (oracle_accumulate(acc, add, n_tensors) != 0)
         return -1;
     return oracle_clip(acc, acc, n_tensors, max_norm, inv_scale, res);
+#endif
 }
 
 /* Out-of-place clip into fp32 buffers: the same decision as oracle_clip, and

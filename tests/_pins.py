@@ -512,4 +512,110 @@ def pin_adamw_skip_and_zero_grads(o):
         assert not storage_bits(t).any()
 
 
+# -- the last microbatch's accumulation folded into the clip ------------------
+
+def _ieee_sum(a: OracleTensor, b: OracleTensor) -> OracleTensor:
+    """The sum of two stored tensors by numpy (fp32, fp16) or torch (bf16),
+    whose additions round the exact sum once to nearest even."""
+    with np.errstate(over="ignore"):        # a sum past the largest finite is inf
+        if a.dtype == "f32":
+            return OracleTensor((a.data + b.data).astype(np.float32), "f32")
+        if a.dtype == "f16":
+            return OracleTensor((a.data + b.data).astype(np.float16), "f16")
+    ta = torch.from_numpy(a.data.view(np.int16).copy()).view(torch.bfloat16)
+    tb = torch.from_numpy(b.data.view(np.int16).copy()).view(torch.bfloat16)
+    return OracleTensor((ta + tb).view(torch.int16).numpy().view(np.uint16).copy(), "bf16")
+
+
+def pin_accumulate_is_the_ieee_sum(o):
+    """Each accumulated element is the stored sum the format's own addition
+    gives (backprop page, 'Accumulation across microbatches': the backward
+    kernels add into the buffer), including overflow to infinity, subnormal
+    sums and the signs of zero."""
+    rng = np.random.default_rng(77)
+    for dt in DTYPES:
+        big = {"f32": 3e38, "f16": 6e4, "bf16": 3e38}[dt]
+        tiny = {"f32": 1e-45, "f16": 6e-8, "bf16": 1e-40}[dt]
+        vals_a = np.concatenate([rng.normal(0, 1, 200), rng.normal(0, 1e-3, 50),
+                                 [big, -big, tiny, -tiny, 0.0, -0.0, 0.0, 1.0]])
+        vals_b = np.concatenate([rng.normal(0, 1, 200), rng.normal(0, 1, 50) * 1e3,
+                                 [big, -big, tiny, tiny, -0.0, -0.0, 0.0, -1.0]])
+        a, b = make(vals_a, dt), make(vals_b, dt)
+        got = o.accumulate([a], [b])[0]
+        want = _ieee_sum(a, b)
+        assert np.array_equal(storage_bits(got), storage_bits(want)), dt
+        # the inputs are left alone
+        assert np.array_equal(storage_bits(a), storage_bits(make(vals_a, dt)))
+
+
+def pin_accumulate_then_clip_worked_example(o):
+    """Contributions [2, 3] and [4, 5] accumulate to the glossary's [6, 8],
+    which the clip at threshold 5 turns into [3, 4]; contributions that cancel
+    leave a zero gradient that passes."""
+    g = golden("worked_example.txt")
+    for dt in DTYPES:
+        outs, r = o.clip_accumulate([make([2, 3], dt)], [make([4, 5], dt)], g["threshold"])
+        assert r.decision == CLIP and r.norm == g["norm"], (dt, r)
+        assert _vals(outs[0]) == g["output"], (dt, _vals(outs[0]))
+        outs, r = o.clip_accumulate([make(g["input"], dt)],
+                                    [make([-v for v in g["input"]], dt)], g["threshold"])
+        assert r.decision == PASS and r.norm == 0.0, (dt, r)
+
+
+def pin_accumulate_before_clip(o):
+    """The clip acts on the accumulated sum, not on each contribution
+    (glossary page, 'Order changes the result'): 10 and -9 accumulate to 1,
+    which a threshold of 5 keeps; clipping the contributions first would give
+    5 - 9 = -4 or 0."""
+    g = golden("accumulation_order.txt")
+    a, b = g["contributions"]
+    for dt in DTYPES:
+        outs, r = o.clip_accumulate([make([a], dt)], [make([b], dt)], g["interval"])
+        assert r.decision == PASS, (dt, r.decision)
+        assert _vals(outs[0]) == [g["clip_of_sum"]], (dt, _vals(outs[0]))
+
+
+def pin_accumulate_bruteforce_exact(o):
+    """Tiny mixed sets: the norm is that of the rounded sums (computed here
+    with exact rationals from the IEEE sums), and every output is the nearest
+    value of its format to the exact clipped sum."""
+    getcontext().prec = 60
+    rng = random.Random(99)
+    for trial in range(30):
+        acc, add = [], []
+        for _ in range(rng.randint(1, 3)):
+            dt = rng.choice(DTYPES)
+            n = rng.randint(0, 5)
+            acc.append(make([rng.gauss(0, 1) for _ in range(n)], dt))
+            add.append(make([rng.gauss(0, 1) for _ in range(n)], dt))
+        sums = [_ieee_sum(a, b) for a, b in zip(acc, add)]
+        inv_scale = rng.choice([1.0, 0.5, 0.3])
+        exact = sum((Fraction(float(v)) * Fraction(inv_scale)) ** 2
+                    for t in sums for v in as_float64(t))
+        norm = (Decimal(exact.numerator) / Decimal(exact.denominator)).sqrt()
+        c = max(float(norm) * rng.choice([0.5, 1.5]), 1e-3)
+        outs, r = o.clip_accumulate(acc, add, c, inv_scale)
+        assert abs(Fraction(r.sumsq) - exact) <= exact / 2 ** 48, trial
+        clip = norm > Decimal(c)
+        assert r.decision == (CLIP if clip else PASS), trial
+        k = (Decimal(c) / norm) if clip else Decimal(1)
+        for t_sum, t_out in zip(sums, outs):
+            for i, v in enumerate(as_float64(t_sum)):
+                wf = Fraction(Decimal(float(v)) * Decimal(inv_scale) * k)
+                lo, mid, hi = _neighbours(t_out, i)
+                d = abs(mid - wf)
+                slack = Fraction(1, 2 ** 40) * abs(wf)
+                assert d <= abs(lo - wf) + slack and d <= abs(hi - wf) + slack, trial
+
+
+def pin_accumulate_skip_keeps_the_sums(o):
+    """A nonfinite contribution stops the update but not the accumulation:
+    the buffer holds the sums (with the infinity), unscaled and unclipped."""
+    acc = [make([1.0, 2.0], "f32"), make([3.0], "bf16")]
+    add = [make([0.5, math.inf], "f32"), make([1.0], "bf16")]
+    outs, r = o.clip_accumulate(acc, add, 1.0, 0.5)
+    assert r.decision == SKIP and r.nonfinite
+    assert _vals(outs[0]) == [1.5, math.inf] and _vals(outs[1]) == [4.0]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -26,6 +26,8 @@ MUTANTS = {
     13: "AdamW weight decay coupled into the gradient",
     14: "AdamW fed the unclipped gradient",
     15: "AdamW second moment with beta1",
+    16: "accumulation subtracts the last microbatch",
+    17: "each contribution clipped before it is added",
 }
 
 
