@@ -66,6 +66,8 @@ def parse_args(argv=None):
                    help="time the fused clip + AdamW step instead of the clip alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-all-cores", action="store_true",
+                   help="skip the all-cores replica timing of the oracle")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU-baseline leg on rank 0")
     return p.parse_args(argv)
@@ -235,6 +237,67 @@ def time_oracle(host, w, reps_budget_s: float):
         if time.perf_counter() - t0 >= reps_budget_s:
             break
     return (time.perf_counter() - t0) / reps, reps, r
+
+
+def _oracle_replica(workload: str, target: int, seconds: float, barrier, results) -> None:
+    """One host core's replica of the oracle (a spawned process): its own
+    seeded sample of the workload, clipped back to back for `seconds` once
+    every replica is ready."""
+    try:
+        import torch
+        torch.set_num_threads(1)
+        import oracle
+        from workloads import WORKLOADS, make_gradset
+        w = WORKLOADS[workload]
+        gs = make_gradset(w, device="cpu")
+        idx, n = reference_sample(gs, target)
+        host = oracle_inputs(type(gs)(w, [gs.tensors[i] for i in idx], gs.spiked))
+        del gs
+        oracle.clip(host, w.max_norm, w.inv_scale)      # load and touch everything once
+    except Exception as exc:   # reported by the parent; the barrier must still be met
+        barrier.wait()
+        results.put(("error", repr(exc)))
+        return
+    barrier.wait()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _, r = oracle.clip(host, w.max_norm, w.inv_scale)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    results.put((time.perf_counter() - t0, reps, n, r.decision_name))
+
+
+def oracle_all_cores(w, seconds: float, target: int = 8 << 20):
+    """Throughput of the unmodified oracle on every host core at once: one
+    spawned process per core, each clipping its own copy of a sample of
+    whole tensors (about `target` elements, starting at the spiked matrix);
+    value = the bytes all replicas moved / the longest replica's time."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(cores)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_replica, args=(w.name, target, seconds, barrier, results))
+             for _ in range(cores)]
+    for p_ in procs:
+        p_.start()
+    out = [results.get(timeout=600) for _ in procs]
+    for p_ in procs:
+        p_.join(timeout=60)
+    errors = [o[1] for o in out if o[0] == "error"]
+    if errors:
+        return {"error": errors[0], "cores": cores}
+    longest = max(o[0] for o in out)
+    nbytes = sum(algorithmic_bytes(o[2], w.elem_bytes, "write" if o[3] != "skip" else "read") * o[1]
+                 for o in out)
+    n = out[0][2]
+    return {"value": round(nbytes / longest / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{cores} single-threaded replicas of the C fp64 oracle, one per host "
+                      f"core, each clipping its own {n}-element sample of the {w.name} set "
+                      f"(whole tensors from the spiked matrix) back to back for {seconds:.0f} s"}
 
 
 def run_reference(args):
@@ -537,7 +600,7 @@ def run_gclip(args):
                "d2h_bytes_per_step": norm_h.element_size() + flag_h.element_size(),
                "ms_per_step": round(e2e_ms, 4)}
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -548,6 +611,8 @@ def run_gclip(args):
                "kind": "oracle",
                "sample": f"the whole {w.name} set ({w.numel} elements), {reps} pass(es), "
                          f"{sec:.2f} s per pass, single-threaded C fp64 oracle"}
+        if not args.no_cpu_all_cores:
+            cpu_all = oracle_all_cores(w, args.cpu_seconds / 2)
 
     for c in clippers:
         c.close()
@@ -585,6 +650,7 @@ def run_gclip(args):
             "e2e": e2e,
             "gpu_launches": args.steps * launches_per_step,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
