@@ -63,6 +63,8 @@ struct gclip_handle {
   SyncWords* d_sync;
   int64_t* d_first;          // first chunk of each tensor, n_tensors + 1 entries
   clip_result_t* d_trec;     // per-tensor records of clip_grad_norm_per_tensor
+  int64_t* d_wlist;          // chunks clip_grad_norm_per_tensor rewrites (n_chunks entries)
+  unsigned int* d_wcount;    // length of that list, entries claimed from it
   std::vector<clip_tensor_desc_t> descs;   // the gradient tensors, as created
   gclip::TensorState* d_states;            // AdamW state table (NULL until attached)
   gclip::TensorState* d_outs;              // fp32 output table (NULL until attached)
@@ -160,7 +162,9 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   const size_t nt = static_cast<size_t>(n_tensors);
   const size_t off_first = round_up(off_sync + sizeof(SyncWords), 256);
   const size_t off_trec = round_up(off_first + (nt + 1) * sizeof(int64_t), 256);
-  const size_t total = round_up(off_trec + (nt ? nt : 1) * sizeof(clip_result_t), 256);
+  const size_t off_wlist = round_up(off_trec + (nt ? nt : 1) * sizeof(clip_result_t), 256);
+  const size_t off_wcount = round_up(off_wlist + (n ? n : 1) * sizeof(int64_t), 256);
+  const size_t total = round_up(off_wcount + 2 * sizeof(unsigned int), 256);
   std::vector<int64_t> first(nt + 1, 0);
   {
     size_t c = 0;
@@ -183,6 +187,8 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   h->d_sync = reinterpret_cast<SyncWords*>(base + off_sync);
   h->d_first = reinterpret_cast<int64_t*>(base + off_first);
   h->d_trec = reinterpret_cast<clip_result_t*>(base + off_trec);
+  h->d_wlist = reinterpret_cast<int64_t*>(base + off_wlist);
+  h->d_wcount = reinterpret_cast<unsigned int*>(base + off_wcount);
 
   int sms = 0, per_sm = 0, coop = 0, l2 = 0;
   e = cudaMemset(h->arena, 0, total);
@@ -628,19 +634,25 @@ extern "C" int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float 
   const int64_t* first = h->d_first;
   clip_result_t* recs = h->d_trec;
   const clip_result_t* crecs = recs;
+  int64_t* wlist = h->d_wlist;
+  const int64_t* cwlist = wlist;
+  unsigned int* wcount = h->d_wcount;
   cudaError_t e = cudaSuccess;
   if (nc > 0) {
-    void* a1[] = {&chunks, &inv_scale, &partials};
+    // Not a programmatic dependent: it empties the write list, which the
+    // previous call's scaling kernel reads until it ends.
+    void* a1[] = {&chunks, &inv_scale, &partials, &wcount};
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_chunk_partials),
                    static_cast<unsigned int>(nc), s, a1, false);
   }
-  void* a2[] = {&cpartials, &first, &max_norm, &inv_scale, &recs, &out_norms, &out_nonfinite_flags};
+  void* a2[] = {&cpartials, &first, &max_norm, &inv_scale, &recs,
+                &out_norms, &out_nonfinite_flags, &wlist, &wcount};
   if (e == cudaSuccess)
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_tensor_final), nt, s, a2, nc > 0);
-  void* a3[] = {&chunks, &nc, &crecs};
+  void* a3[] = {&chunks, &cwlist, &wcount, &crecs};
   if (e == cudaSuccess && nc > 0)
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_scale_per_tensor),
-                   static_cast<unsigned int>(nc), s, a3, true);
+                   static_cast<unsigned int>(h->grid_persistent), s, a3, true);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GCLIP_ERR_CUDA;

@@ -271,46 +271,81 @@ __global__ void __launch_bounds__(kThreads, 5) k_grad_norm_accumulate(const Norm
 // ---------------------------------------------------------------------------
 // Per-tensor clipping: each tensor clipped by its own norm.  One block per
 // chunk writes the chunk's sum of squares; one block per tensor reduces its
-// chunks' sums (the same fixed order as the final reduction) and decides;
-// one block per chunk scales with its tensor's multiplier.
+// chunks' sums (the same fixed order as the final reduction), decides, and
+// lists its chunks if they are to be rewritten; a wave of blocks scales the
+// listed chunks, each with its tensor's multiplier.
 
 __global__ void __launch_bounds__(kThreads) k_chunk_partials(const clip_chunk_t* __restrict__ chunks,
                                                              float inv_scale,
-                                                             float2* __restrict__ partials) {
+                                                             float2* __restrict__ partials,
+                                                             unsigned int* wcount) {
   __shared__ FF red[kWarps];
   asm volatile("griddepcontrol.launch_dependents;");
+  // Launched after the previous call's scaling kernel has finished (no
+  // programmatic dependence), so the write list can be emptied here.
+  if (blockIdx.x == 0 && threadIdx.x == 0) wcount[0] = wcount[1] = 0u;
   const FF acc = chunk_sumsq<HintMem>(chunks[blockIdx.x], inv_scale, red, policy_evict_first());
   if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
 }
 
+// One block per tensor: the tensor's norm and decision, and, when its
+// elements are to be rewritten, its chunks appended to the write list (in
+// whatever order the tensors finish: each chunk is scaled on its own, so the
+// order changes nothing in the results).
 __global__ void __launch_bounds__(kThreads) k_tensor_final(const float2* __restrict__ partials,
                                                            const int64_t* __restrict__ first,
                                                            float max_norm, float inv_scale,
                                                            clip_result_t* recs, float* out_norms,
-                                                           int32_t* out_flags) {
+                                                           int32_t* out_flags,
+                                                           int64_t* __restrict__ wlist,
+                                                           unsigned int* wcount) {
   __shared__ FF red[kWarps];
+  __shared__ int64_t s_base;
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
-  const FF acc = reduce_partials(partials + first[t], first[t + 1] - first[t], red);
-  if (threadIdx.x == 0)
+  const int64_t c0 = first[t], nc = first[t + 1] - c0;
+  const FF acc = reduce_partials(partials + c0, nc, red);
+  if (threadIdx.x == 0) {
     decide_write(acc, max_norm, inv_scale, recs + t, out_norms ? out_norms + t : nullptr,
                  out_flags ? out_flags + t : nullptr);
+    const clip_result_t& r = recs[t];
+    s_base = must_write(r.decision, r.coef_hi, r.coef_lo) && nc > 0
+                 ? static_cast<int64_t>(atomicAdd(wcount, static_cast<unsigned int>(nc)))
+                 : -1;
+  }
+  __syncthreads();
+  if (s_base >= 0)
+    for (int64_t k = threadIdx.x; k < nc; k += kThreads) wlist[s_base + k] = c0 + k;
 }
 
+// One resident wave of blocks scales the listed chunks: block b takes entry
+// b first, then claims entries from a counter until the list is done
+// (wcount[0] = the list's length, wcount[1] = entries claimed beyond the
+// first wave).  A sparse list costs one wave of short blocks; a full one is
+// balanced by the claims.
 __global__ void __launch_bounds__(kThreads) k_scale_per_tensor(const clip_chunk_t* __restrict__ chunks,
-                                                               int64_t n_chunks,
+                                                               const int64_t* __restrict__ wlist,
+                                                               unsigned int* wcount,
                                                                const clip_result_t* recs) {
+  __shared__ unsigned int s_k;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
-  const clip_result_t* r = recs + (c.meta >> 8);
-  const int decision = __ldcg(&r->decision);
-  const float chi = __ldcg(&r->coef_hi), clo = __ldcg(&r->coef_lo);
-  if (!must_write(decision, chi, clo)) return;
+  const unsigned int n = __ldcg(wcount);
+  if (blockIdx.x >= n) return;
   // Real work follows: let the next dependent launch be scheduled now
   // (blocks that write nothing trigger by exiting).
   asm volatile("griddepcontrol.launch_dependents;");
-  chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
+  const uint64_t pol = policy_evict_first();
+  unsigned int k = blockIdx.x;
+  while (k < n) {
+    const clip_chunk_t c = chunks[__ldcg(wlist + k)];
+    const clip_result_t* r = recs + (c.meta >> 8);
+    chunk_scale<HintMem>(c, __ldcg(&r->coef_hi), __ldcg(&r->coef_lo), pol);
+    if (threadIdx.x == 0) s_k = gridDim.x + atomicAdd(wcount + 1, 1u);
+    __syncthreads();
+    k = s_k;
+    __syncthreads();  // s_k is written again in the next round
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -89,3 +89,30 @@ def test_no_tensors():
     with g.GradClipper([]) as c:
         c.clip_per_tensor_(1.0)
         assert c.per_tensor_results() == []
+
+
+def test_repeated_calls_reuse_the_write_list():
+    """Calls on one clipper: everything rewritten (unscale), then nothing
+    (every tensor passes at multiplier 1), then a few tensors clip."""
+    gs = make_gradset("andrea14m", device=dev())
+    with g.GradClipper(gs.tensors) as c:
+        for max_norm, inv_scale, expect_writes in ((1e6, 0.5, True), (1e6, 1.0, False),
+                                                    (0.02, 1.0, True)):
+            before = [to_oracle(t) for t in gs.tensors]
+            c.clip_per_tensor_(max_norm, inv_scale)
+            recs = c.per_tensor_results()
+            want, rs = oracle.default().clip_per_tensor(before, max_norm, inv_scale)
+            wrote = False
+            for b, t, w, r, rec in zip(before, gs.tensors, want, rs, recs):
+                assert rec["decision"] == r.decision
+                got = to_oracle(t)
+                assert int(ulp_distance(got, w).max()) <= ULP_TOL[w.dtype]
+                wrote |= not np.array_equal(storage_bits(got), storage_bits(b))
+            assert wrote == expect_writes, (max_norm, inv_scale)
+
+
+def test_only_empty_tensors():
+    ts = [torch.empty(0, device=dev()), torch.empty(0, device=dev(), dtype=torch.float16)]
+    with g.GradClipper(ts) as c:
+        norms, flags = c.clip_per_tensor_(1.0, 0.5)
+        assert norms.tolist() == [0.0, 0.0] and flags.tolist() == [0, 0]
