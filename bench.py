@@ -45,7 +45,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=3200)
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["gclip", "reference"], default="gclip")
-    p.add_argument("--variant", choices=["split", "persistent", "split_tma", "persistent_tma"],
+    p.add_argument("--variant", choices=["split", "persistent", "split_tma", "persistent_tma", "split_wave"],
                    default="split")
     p.add_argument("--workload", default="andrea120m")
     p.add_argument("--pool", type=int, default=32, help="distinct gradient sets per timed run")
@@ -551,7 +551,8 @@ def run_gclip(args):
     else:
         tma = args.variant.endswith("tma")
         shares = {("k_norm_tma" if tma else "k_grad_norm_partial"): (seg_ms[0], w.numel * w.elem_bytes),
-                  ("k_scale_tma" if tma else "k_grad_scale"): (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
+                  ("k_scale_tma" if tma else "k_grad_scale_wave" if args.variant == "split_wave"
+                   else "k_grad_scale"): (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
         kernel = max(shares, key=lambda k: shares[k][0])
         k_ms, k_bytes = shares[kernel]
     peaks = {}

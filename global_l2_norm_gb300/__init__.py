@@ -36,7 +36,8 @@ DTYPE_CODES = {torch.float32: GCLIP_F32, torch.float16: GCLIP_F16,
 VARIANTS = {"split": GCLIP_VARIANT_SPLIT,
             "persistent": GCLIP_VARIANT_PERSISTENT,
             "split_tma": _abi.GCLIP_VARIANT_SPLIT_TMA,
-            "persistent_tma": _abi.GCLIP_VARIANT_PERSISTENT_TMA}
+            "persistent_tma": _abi.GCLIP_VARIANT_PERSISTENT_TMA,
+            "split_wave": _abi.GCLIP_VARIANT_SPLIT_WAVE}
 
 
 def build(force: bool = False) -> str:

@@ -33,6 +33,7 @@ GCLIP_VARIANT_SPLIT = 0
 GCLIP_VARIANT_PERSISTENT = 1
 GCLIP_VARIANT_SPLIT_TMA = 2
 GCLIP_VARIANT_PERSISTENT_TMA = 3
+GCLIP_VARIANT_SPLIT_WAVE = 4
 
 GCLIP_CHUNK_BYTES = 32768
 GCLIP_MAX_TENSORS = 1 << 24

@@ -108,6 +108,7 @@ gclip::NormArgs norm_args(gclip_handle* h, int32_t grid, float max_norm, float i
   a.n_chunks = h->n_chunks;
   a.block_sums = h->d_partials;
   a.arrive = &h->d_sync->arrive;
+  a.work = &h->d_sync->work;
   a.expected = static_cast<unsigned int>(grid) + extra;
   a.max_norm = max_norm;
   a.inv_scale = inv_scale;
@@ -232,6 +233,23 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
 
 namespace {
 
+// The in-place scaling pass of the split variants, after the norm pass:
+// one block per chunk, or (SPLIT_WAVE) one resident wave that claims chunks.
+cudaError_t launch_scale(clip_handle_t h, cudaStream_t s, bool pdl) {
+  const clip_chunk_t* chunks = h->d_chunks;
+  int64_t nc = h->n_chunks;
+  const clip_result_t* cres = h->d_result;
+  if (h->variant == GCLIP_VARIANT_SPLIT_WAVE) {
+    unsigned int* work = &h->d_sync->work;
+    void* args[] = {&chunks, &nc, &cres, &work};
+    return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale_wave),
+                      static_cast<unsigned int>(h->grid_persistent), s, args, pdl);
+  }
+  void* args[] = {&chunks, &nc, &cres};
+  return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale),
+                    static_cast<unsigned int>(nc), s, args, pdl);
+}
+
 // Enqueue one clip.  `events` (may be NULL) are recorded between the steps;
 // programmatic dependent launch is used only when no events are recorded.
 int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
@@ -251,7 +269,7 @@ int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
     void* args[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm, &out_flag};
     if (e == cudaSuccess)
       e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, args, false);
-  } else if (h->variant == GCLIP_VARIANT_SPLIT) {
+  } else if (h->variant == GCLIP_VARIANT_SPLIT || h->variant == GCLIP_VARIANT_SPLIT_WAVE) {
     gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag, 0);
     void* a1[] = {&a};
     if (e == cudaSuccess)
@@ -259,12 +277,7 @@ int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
                      static_cast<unsigned int>(h->grid_persistent), s, a1, pdl);
     mark(1);
     mark(2);
-    const clip_chunk_t* chunks = h->d_chunks;
-    const clip_result_t* cres = h->d_result;
-    void* a3[] = {&chunks, &nc, &cres};
-    if (e == cudaSuccess)
-      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale),
-                     static_cast<unsigned int>(nc), s, a3, pdl);
+    if (e == cudaSuccess) e = launch_scale(h, s, pdl);
   } else if (h->variant == GCLIP_VARIANT_SPLIT_TMA) {
     gclip::NormArgs a = norm_args(h, h->grid_tma, max_norm, inv_scale, out_norm, out_flag, 0);
     void* a1[] = {&a};
@@ -364,7 +377,7 @@ extern "C" int clip_destroy(clip_handle_t h) {
 
 extern "C" int clip_set_variant(clip_handle_t h, int32_t variant) {
   if (h == nullptr) return GCLIP_ERR_INVALID_ARG;
-  if (variant < GCLIP_VARIANT_SPLIT || variant > GCLIP_VARIANT_PERSISTENT_TMA)
+  if (variant < GCLIP_VARIANT_SPLIT || variant > GCLIP_VARIANT_SPLIT_WAVE)
     return GCLIP_ERR_INVALID_ARG;
   const bool coop = variant == GCLIP_VARIANT_PERSISTENT || variant == GCLIP_VARIANT_PERSISTENT_TMA;
   const int32_t grid = (variant == GCLIP_VARIANT_SPLIT_TMA || variant == GCLIP_VARIANT_PERSISTENT_TMA)
@@ -553,12 +566,7 @@ extern "C" int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float 
     void* a1[] = {&a, &adds};
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_accumulate),
                    static_cast<unsigned int>(h->grid_persistent), s, a1, true);
-    const clip_chunk_t* chunks = h->d_chunks;
-    const clip_result_t* cres = h->d_result;
-    void* a2[] = {&chunks, &nc, &cres};
-    if (e == cudaSuccess)
-      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale),
-                     static_cast<unsigned int>(nc), s, a2, true);
+    if (e == cudaSuccess) e = launch_scale(h, s, true);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

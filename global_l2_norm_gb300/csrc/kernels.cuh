@@ -51,6 +51,34 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __r
   chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
 }
 
+// The scaling pass as one resident wave: block b scales chunk b (counted from
+// the highest, as above), then claims further chunks from a counter that the
+// norm pass's last block zeroed, asking for the next one before scaling the
+// current one.  When nothing is written only this wave has to retire.
+__global__ void __launch_bounds__(kThreads) k_grad_scale_wave(const clip_chunk_t* __restrict__ chunks,
+                                                              int64_t n_chunks,
+                                                              const clip_result_t* res,
+                                                              unsigned int* work) {
+  __shared__ unsigned int s_next[2];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int decision = res->decision;
+  const float chi = res->coef_hi, clo = res->coef_lo;
+  if (!must_write(decision, chi, clo)) return;
+  asm volatile("griddepcontrol.launch_dependents;");
+  const uint64_t pol = policy_evict_first();
+  int64_t k = blockIdx.x;
+  int par = 0;
+  while (k < n_chunks) {
+    // Two slots: a slot is written again only after every thread has
+    // passed the barrier that follows its read.
+    if (threadIdx.x == 0) s_next[par] = gridDim.x + atomicAdd(work, 1u);
+    chunk_scale<HintMem>(chunks[n_chunks - 1 - k], chi, clo, pol);
+    __syncthreads();
+    k = s_next[par];
+    par ^= 1;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Fused clip + AdamW: after the norm pass, one pass over gradients and state
 // that forms the clipped gradient in registers and updates w, m, v.

@@ -308,6 +308,7 @@ struct NormArgs {
   int64_t n_chunks;
   float2* block_sums;     // G entries
   unsigned int* arrive;   // blocks done with the norm pass in this call
+  unsigned int* work;     // chunks the scaling pass claims in this call
   unsigned int expected;  // G, plus the test hook's extra arrivals
   float max_norm;
   float inv_scale;
@@ -344,6 +345,7 @@ __device__ __forceinline__ bool norm_arrive(const NormArgs& a, FF bsum, FF* red,
                red);
   if (threadIdx.x == 0) {
     *a.arrive = 0u;  // every block has arrived: rearm for the next call
+    *a.work = 0u;    // no scaling block claims before the record is out
     __threadfence();
   }
   return true;

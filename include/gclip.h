@@ -72,6 +72,12 @@ extern "C" {
                                        shared memory by bulk (TMA) copies  */
 #define GCLIP_VARIANT_PERSISTENT_TMA 3  /* as PERSISTENT, staged by bulk
                                        (TMA) copies                         */
+#define GCLIP_VARIANT_SPLIT_WAVE 4  /* as SPLIT, with the scaling done by one
+                                       resident wave of blocks that claim
+                                       chunks from a counter: slower by
+                                       about 0.5% when every element is
+                                       written, faster when nothing is
+                                       (few blocks to retire)               */
 
 /* One gradient tensor: `numel` elements of format `dtype`, contiguous, in
  * device memory at `ptr` (aligned to the element size).  `reserved` must be
@@ -198,8 +204,9 @@ int clip_grad_norm_profiled(clip_handle_t h, float max_norm, float inv_scale,
 int clip_destroy(clip_handle_t h);
 
 /* clip_set_variant -- choose one of the GCLIP_VARIANT_* values for later
- * calls (GCLIP_VARIANT_SPLIT is the default).  SPLIT and PERSISTENT compute
- * bit-identical norms and outputs, and so do SPLIT_TMA and PERSISTENT_TMA;
+ * calls (GCLIP_VARIANT_SPLIT is the default).  SPLIT, SPLIT_WAVE and
+ * PERSISTENT compute bit-identical norms and outputs, and so do SPLIT_TMA and
+ * PERSISTENT_TMA;
  * the two pairs sum in a different (fixed) order, so their norms can differ
  * in the last bits.  Returns GCLIP_ERR_INVALID_ARG for an unknown variant,
  * GCLIP_ERR_UNSUPPORTED if the device cannot launch cooperative kernels. */
@@ -415,8 +422,9 @@ int clip_attach_addend(clip_handle_t h, const void *const *addends, int32_t n_te
  * addends with the format's own addition and then calling clip_grad_norm
  * with the split variant.  The sums are stored whatever the decision: on
  * SKIP (a nonfinite sum) the gradients hold the unscaled, unclipped sums.
- * Two launches (the norm pass with the addition, then the scaling),
- * whatever clip_set_variant chose; asynchronous, no allocation.  Returns
+ * Two launches (the norm pass with the addition, then the scaling: by the
+ * claiming wave under GCLIP_VARIANT_SPLIT_WAVE, else one block per chunk);
+ * asynchronous, no allocation.  Returns
  * GCLIP_OK; GCLIP_ERR_INVALID_ARG (NULL handle, no addends attached, bad
  * max_norm / inv_scale); GCLIP_ERR_CUDA. */
 int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float inv_scale,

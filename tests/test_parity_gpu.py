@@ -14,7 +14,7 @@ from workloads import WORKLOADS, make_gradset
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["split", "persistent", "split_tma", "persistent_tma"]
+VARIANTS = ["split", "persistent", "split_tma", "persistent_tma", "split_wave"]
 TD = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -243,7 +243,8 @@ def test_rejects_host_memory_descriptor():
 
 # -- determinism ----------------------------------------------------------------
 
-@pytest.mark.parametrize("pair", [("split", "persistent"), ("split_tma", "persistent_tma")])
+@pytest.mark.parametrize("pair", [("split", "persistent"), ("split_tma", "persistent_tma"),
+                                  ("split", "split_wave")])
 def test_bit_identical_runs_and_variants(pair):
     """20 runs alternating the two variants of one engine: the same norm,
     sum of squares and multiplier bit for bit, and the same outputs."""
