@@ -393,7 +393,10 @@ def run_gclip(args):
     if args.l2_keep_mb is not None:
         for c in clippers:
             c.set_l2_keep(int(args.l2_keep_mb * (1 << 20)))
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    device_info = {"name": props.name, "sms": props.multi_processor_count, "l2_bytes": l2,
+                   "hbm_bytes": props.total_memory}
     flush = torch.empty(2 * l2 + (1 << 20), dtype=torch.uint8, device=dev)
 
     writes = True
@@ -654,6 +657,7 @@ def run_gclip(args):
                             else "accumulate" if args.accumulate
                             else args.variant), "pool": P,
                 "l2_keep_mb": args.l2_keep_mb, "written_elements": written, "parallelism": f"replicas x{world}",
+                "device": device_info,
                 "l2": ("warm: one set re-read from L2, no flush" if args.warm else
                        "inputs larger than L2 (one set per step, pool of distinct sets); "
                        "L2 flushed before each timed run"),
