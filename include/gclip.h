@@ -350,8 +350,11 @@ int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
  * when tensor t holds a NaN/inf (that tensor alone is skipped).  Empty
  * tensors have norm 0.  out_norms, out_nonfinite_flags: device arrays of one
  * entry per tensor, each may be NULL.  The per-tensor records go to the
- * handle (clip_read_per_tensor).  Three launches (chunk sums, one block per
- * tensor, scaling); asynchronous, no allocation.  Returns GCLIP_OK,
+ * handle (clip_read_per_tensor).  Three launches (chunk sums; one block per
+ * tensor, which decides and lists the chunks to rewrite; one wave of blocks
+ * scaling the listed chunks); asynchronous, no allocation.  Consecutive
+ * per-tensor calls on one handle must be issued in stream order (the chunk
+ * list is the handle's).  Returns GCLIP_OK,
  * GCLIP_ERR_INVALID_ARG (NULL handle, bad max_norm / inv_scale) or
  * GCLIP_ERR_CUDA. */
 int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float inv_scale,
