@@ -48,6 +48,7 @@ using gclip::SyncWords;
 struct gclip_handle {
   int device;
   int64_t n_chunks;
+  int64_t total_bytes;       // bytes of all gradients
   int64_t keep_from;         // first chunk the norm pass reads with evict_last
   int64_t l2_bytes;          // L2 size of the device
   int32_t variant;
@@ -116,6 +117,7 @@ gclip::NormArgs norm_args(gclip_handle* h, int32_t grid, float max_norm, float i
   a.out_norm = out_norm;
   a.out_flag = out_flag;
   a.keep_from = h->keep_from;
+  a.resident = h->total_bytes <= h->l2_bytes / 2 ? 1 : 0;
   return a;
 }
 
@@ -149,6 +151,8 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
     return GCLIP_ERR_CUDA;
   }
   h->n_chunks = static_cast<int64_t>(chunks.size());
+  for (int32_t t = 0; t < n_tensors; ++t)
+    h->total_bytes += descs[t].numel * (descs[t].dtype == GCLIP_F32 ? 4 : 2);
   h->variant = GCLIP_VARIANT_SPLIT;
   h->descs.assign(descs, descs + n_tensors);
   h->timeout_ns = gclip::kDefaultTimeoutNs;

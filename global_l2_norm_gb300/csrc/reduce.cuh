@@ -316,10 +316,13 @@ struct NormArgs {
   float* out_norm;
   int32_t* out_flag;
   int64_t keep_from;      // chunks from here on are read with evict_last
+  int resident;           // the set fits in half of L2: the rest is read with evict_normal
 };
 
 __device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
-  const uint64_t pol_first = policy_evict_first();
+  // A set that fits in L2 may stay there for the next call; a larger one is
+  // streamed through without displacing anything.
+  const uint64_t pol_first = a.resident ? policy_evict_normal() : policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
   FF acc = {0.f, 0.f};
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {

@@ -261,8 +261,11 @@ const char *clip_status_string(int32_t code);
  * policy, so that the scaling pass finds them in L2 instead of HBM.  The
  * default is 0 (off): on the ANDREA-120M fp32 set the hint moved ~50 MB of
  * the scaling pass's reads into L2 but did not shorten the clip.  Rounded
- * down to whole chunks.  Affects timing only, never results.  Returns GCLIP_OK or
- * GCLIP_ERR_INVALID_ARG (NULL handle, negative bytes). */
+ * down to whole chunks.  The other chunks are read with evict_first, except
+ * in sets that fit in half of the device's L2, which are read with the normal
+ * policy so that a set clipped again soon is still in L2.  Affects timing
+ * only, never results.  Returns GCLIP_OK or GCLIP_ERR_INVALID_ARG (NULL
+ * handle, negative bytes). */
 int clip_set_l2_keep(clip_handle_t h, int64_t bytes);
 
 /* clip_debug_barrier -- test hook for the single-launch variant's bounded
