@@ -337,19 +337,25 @@ __device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
 __device__ __forceinline__ bool norm_arrive(const NormArgs& a, FF bsum, FF* red, int* s_flag) {
   if (threadIdx.x == 0) {
     a.block_sums[blockIdx.x] = make_float2(bsum.hi, bsum.lo);
-    __threadfence();
-    const unsigned int t = atomicAdd(a.arrive, 1u);
+    // One acquire-release ticket: the release publishes this block's sum
+    // with the increment; the acquire in the block that takes the last
+    // ticket makes every earlier block's sum visible to it (the increments
+    // form one release sequence), and the barrier below passes that on to
+    // the block's other threads.
+    unsigned int t;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(a.arrive) : "memory");
     *s_flag = (t + 1u == a.expected);
   }
   __syncthreads();
   if (!*s_flag) return false;
-  __threadfence();
   final_reduce(a.block_sums, gridDim.x, a.max_norm, a.inv_scale, a.res, a.out_norm, a.out_flag,
                red);
   if (threadIdx.x == 0) {
+    // No fence: the end of the kernel orders these stores and the record
+    // before the dependent launch; the single-launch kernels fence before
+    // they release the other blocks.
     *a.arrive = 0u;  // every block has arrived: rearm for the next call
     *a.work = 0u;    // no scaling block claims before the record is out
-    __threadfence();
   }
   return true;
 }

@@ -396,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_clip_persistent_tma(const NormA
 
   if (published) {
     if (threadIdx.x == 0) {
+      __threadfence();  // the record before the generation that releases the others
       atomicAdd(&sync->gen, 1u);
       s_go = 1;
     }
