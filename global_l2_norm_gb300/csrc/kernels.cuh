@@ -228,16 +228,30 @@ __device__ __forceinline__ void to_f32_chunk(const clip_chunk_t& c, const Tensor
   const uint64_t pol = policy_evict_first();
   const uint4* gv = reinterpret_cast<const uint4*>(sp.body);
   if ((reinterpret_cast<uint64_t>(out + sp.head) & 15u) == 0) {
-    for (uint32_t i = threadIdx.x; i < sp.nvec; i += kThreads) {
-      float x[8];
-      widen_vec<DT>(HintMem::ld_scale(gv + i, pol), x);
-      float4* o = reinterpret_cast<float4*>(out + sp.head + i * E);
+    // fp32: four loads in flight per thread; fp16/bf16 (two 16-byte stores
+    // per load): one (measured: batching the 16-bit formats was slower).
+    constexpr int U = Fmt<DT>::kBytes == 4 ? 4 : 1;
+    for (uint32_t base = threadIdx.x; base < sp.nvec; base += U * kThreads) {
+      uint4 v[U];
 #pragma unroll
-      for (uint32_t q = 0; q < E; q += 4)
-        __stcs(o + q / 4, make_float4(Fmt<GCLIP_F32>::scale1(x[q], chi, clo),
-                                      Fmt<GCLIP_F32>::scale1(x[q + 1], chi, clo),
-                                      Fmt<GCLIP_F32>::scale1(x[q + 2], chi, clo),
-                                      Fmt<GCLIP_F32>::scale1(x[q + 3], chi, clo)));
+      for (int u = 0; u < U; ++u) {
+        const uint32_t i = base + u * kThreads;
+        v[u] = i < sp.nvec ? HintMem::ld_scale(gv + i, pol) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t i = base + u * kThreads;
+        if (i >= sp.nvec) break;
+        float x[8];
+        widen_vec<DT>(v[u], x);
+        float4* o = reinterpret_cast<float4*>(out + sp.head + i * E);
+#pragma unroll
+        for (uint32_t q = 0; q < E; q += 4)
+          __stcs(o + q / 4, make_float4(Fmt<GCLIP_F32>::scale1(x[q], chi, clo),
+                                        Fmt<GCLIP_F32>::scale1(x[q + 1], chi, clo),
+                                        Fmt<GCLIP_F32>::scale1(x[q + 2], chi, clo),
+                                        Fmt<GCLIP_F32>::scale1(x[q + 3], chi, clo)));
+      }
     }
   } else {
     for (uint32_t j = sp.head + threadIdx.x; j < sp.tail_start; j += kThreads)
