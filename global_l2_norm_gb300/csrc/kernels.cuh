@@ -347,10 +347,11 @@ __global__ void __launch_bounds__(kThreads) k_tensor_final(const float2* __restr
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int64_t c0 = first[t], nc = first[t + 1] - c0;
+  const unsigned int calls = threadIdx.x == 0 ? __ldcg(&recs[t].calls) : 0u;
   const FF acc = reduce_partials(partials + c0, nc, red);
   if (threadIdx.x == 0) {
     decide_write(acc, max_norm, inv_scale, recs + t, out_norms ? out_norms + t : nullptr,
-                 out_flags ? out_flags + t : nullptr);
+                 out_flags ? out_flags + t : nullptr, calls);
     const clip_result_t& r = recs[t];
     s_base = must_write(r.decision, r.coef_hi, r.coef_lo) && nc > 0
                  ? static_cast<int64_t>(atomicAdd(wcount, static_cast<unsigned int>(nc)))

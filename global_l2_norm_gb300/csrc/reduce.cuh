@@ -233,20 +233,18 @@ __device__ __forceinline__ bool must_write(int decision, float chi, float clo) {
 
 __device__ FF reduce_partials(const float2* partials, int64_t n, FF* red) {
   FF acc = {0.f, 0.f};
-  int64_t c = threadIdx.x;
-  for (; c + 3 * kThreads < n; c += 4 * kThreads) {
-    const float2 p0 = __ldcg(partials + c);
-    const float2 p1 = __ldcg(partials + c + kThreads);
-    const float2 p2 = __ldcg(partials + c + 2 * kThreads);
-    const float2 p3 = __ldcg(partials + c + 3 * kThreads);
-    acc = ff_add(acc, FF{p0.x, p0.y});
-    acc = ff_add(acc, FF{p1.x, p1.y});
-    acc = ff_add(acc, FF{p2.x, p2.y});
-    acc = ff_add(acc, FF{p3.x, p3.y});
-  }
-  for (; c < n; c += kThreads) {
-    const float2 p = __ldcg(partials + c);
-    acc = ff_add(acc, FF{p.x, p.y});
+  // Up to four entries loaded at once, then added in increasing index order:
+  // thread t's sum is always entries t, t + kThreads, t + 2 kThreads, ...
+  for (int64_t c = threadIdx.x; c < n; c += 4 * kThreads) {
+    float2 p[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = c + u * kThreads;
+      p[u] = i < n ? __ldcg(partials + i) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c + u * kThreads < n) acc = ff_add(acc, FF{p[u].x, p[u].y});
   }
   return block_reduce(acc, red);
 }
@@ -254,7 +252,7 @@ __device__ FF reduce_partials(const float2* partials, int64_t n, FF* red) {
 // The norm, flag, decision and multiplier from the float-float sum of
 // squares S = hi + lo (thread 0).
 __device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_result_t* res,
-                             float* out_norm, int32_t* out_flag) {
+                             float* out_norm, int32_t* out_flag, unsigned int calls) {
   const double S = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
   const bool nonfinite = !isfinite(acc.hi) || !isfinite(acc.lo) || S > static_cast<double>(FLT_MAX);
   const double norm = sqrt(S);
@@ -279,7 +277,7 @@ __device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_resul
   res->coef_lo = clo;
   res->sumsq_hi = acc.hi;
   res->sumsq_lo = acc.lo;
-  res->calls = res->calls + 1u;
+  res->calls = calls + 1u;  // `calls`: the count read before the reduction
   if (out_norm) *out_norm = norm_f;
   if (out_flag) *out_flag = nonfinite ? 1 : 0;
 }
@@ -287,8 +285,11 @@ __device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_resul
 __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max_norm,
                              float inv_scale, clip_result_t* res, float* out_norm,
                              int32_t* out_flag, FF* red) {
+  // The record's call count, loaded now so that its latency overlaps the
+  // reduction instead of following it.
+  const unsigned int calls = threadIdx.x == 0 ? __ldcg(&res->calls) : 0u;
   const FF acc = reduce_partials(partials, n_chunks, red);
-  if (threadIdx.x == 0) decide_write(acc, max_norm, inv_scale, res, out_norm, out_flag);
+  if (threadIdx.x == 0) decide_write(acc, max_norm, inv_scale, res, out_norm, out_flag, calls);
 }
 
 // ---------------------------------------------------------------------------
