@@ -1,6 +1,7 @@
-// kernels.cuh -- the register-engine kernels: the split variant, fused clip
-// + AdamW, the out-of-place fp32 clip, per-tensor clipping and the
-// single-launch variant.  Included by gclip.cu only.
+// kernels.cuh -- the register-engine kernels: the split variant (and its
+// claiming-wave scaling pass), fused clip + AdamW, the out-of-place fp32
+// clip, the accumulation epilogue, per-tensor clipping and the single-launch
+// variant.  Included by gclip.cu only.
 #pragma once
 
 #include "reduce.cuh"

@@ -1,6 +1,7 @@
 // reduce.cuh -- the arithmetic of the norm: per-thread sums of squares of a
-// chunk, the fixed block tree, the scaling of a chunk, the final reduction
-// with the decision in double, and the norm pass shared by both variants.
+// chunk (plain, or with the last microbatch added in), the fixed block tree,
+// the scaling of a chunk, the final reduction with the decision in double,
+// and the norm pass shared by the register-engine variants.
 // Included by gclip.cu only.
 #pragma once
 
@@ -293,7 +294,8 @@ __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max
 }
 
 // ---------------------------------------------------------------------------
-// The norm pass of the handle-based clip, shared by both variants.
+// The norm pass of the handle-based clip, shared by the register-engine
+// variants (split, split_wave, single launch).
 //
 // A grid of G blocks (G fixed per handle: the co-resident count of the
 // single-launch kernel, at most the number of chunks).  Block b takes chunks
