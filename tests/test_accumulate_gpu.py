@@ -192,3 +192,20 @@ def test_attach_rejects_bad_addends():
         y = torch.empty(64, device=dev())
         with pytest.raises(g.GclipError):
             c.attach_addend([y[:32], y[16:48]])                           # addends overlap
+
+
+def test_twenty_thousand_small_tensors():
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    sizes = torch.randint(0, 10, (20000,), generator=gen).tolist()
+    for i in range(0, 20000, 1000):
+        sizes[i] = 3000 + i
+    gbuf = torch.randn(sum(sizes) + 20000, generator=gen).to(dev())
+    abuf = torch.randn(sum(sizes) + 40000, generator=gen).to(dev())
+    grads, adds, go, ao = [], [], 0, 1
+    for k in sizes:
+        grads.append(gbuf[go:go + k])
+        adds.append(abuf[ao:ao + k])
+        go += k + 1
+        ao += k + 2
+    r, _ = run(grads, adds, 10.0, 0.5)
+    assert r.decision == oracle.CLIP

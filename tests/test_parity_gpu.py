@@ -346,3 +346,31 @@ def test_norm_is_the_rounded_exact_norm(name):
     want = np.float32(r.norm)
     ulps = abs(int(np.array([got]).view(np.int32)[0]) - int(np.array([want]).view(np.int32)[0]))
     assert ulps <= 1, (float(got), float(want), ulps)
+
+
+# -- many small tensors -------------------------------------------------------------
+
+def many_small(seed, n=20000, dt=torch.float32):
+    """n tensors of 0..9 elements (plus every 1000th of a few thousand), cut
+    out of one buffer at odd element offsets: most chunks are only a head or
+    a tail, with no vector body."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    sizes = torch.randint(0, 10, (n,), generator=gen).tolist()
+    for i in range(0, n, 1000):
+        sizes[i] = 3000 + i
+    buf = torch.randn(sum(sizes) + n, generator=gen).to(dt).to(dev())
+    ts, pos = [], 0
+    for k in sizes:
+        ts.append(buf[pos:pos + k])
+        pos += k + 1
+    return ts
+
+
+@pytest.mark.parametrize("variant", ["split", "persistent", "split_tma"])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_twenty_thousand_small_tensors(variant, dt):
+    ts = many_small(5, dt=dt)
+    before = host_copies(ts)
+    rec = gpu_clip(ts, 10.0, 0.5, variant)
+    compare(before, ts, rec, 10.0, 0.5, f"many-{variant}")
+    assert rec["decision"] == g.GCLIP_DECISION_CLIP

@@ -116,3 +116,17 @@ def test_only_empty_tensors():
     with g.GradClipper(ts) as c:
         norms, flags = c.clip_per_tensor_(1.0, 0.5)
         assert norms.tolist() == [0.0, 0.0] and flags.tolist() == [0, 0]
+
+
+def test_twenty_thousand_small_tensors():
+    gen = torch.Generator(device="cpu").manual_seed(6)
+    sizes = torch.randint(0, 10, (20000,), generator=gen).tolist()
+    for i in range(0, 20000, 1000):
+        sizes[i] = 3000 + i
+    buf = torch.randn(sum(sizes) + 20000, generator=gen).to(dev())
+    ts, pos = [], 0
+    for k in sizes:
+        ts.append(buf[pos:pos + k])
+        pos += k + 1
+    d = check(ts, 2.0, 0.5)
+    assert oracle.CLIP in d and oracle.PASS in d
