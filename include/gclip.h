@@ -169,7 +169,8 @@ int clip_create(const clip_tensor_desc_t *descs, int32_t n_tensors,
  *
  * The sum is taken in a fixed order (per chunk, then over chunks) with a
  * float-float accumulator, so the norm is bit-identical from run to run and
- * between the two variants.
+ * between the SPLIT, SPLIT_WAVE and PERSISTENT variants (the two TMA variants
+ * share another fixed order).
  *
  * max_norm: threshold c, finite and > 0.  inv_scale: finite and > 0.
  * out_norm: device float, may be NULL; receives the norm (fp32).
