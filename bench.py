@@ -113,12 +113,15 @@ def aggregate(elapsed_ms: float, units: float, world: int, reduce_max=None):
 
 
 def source_digest() -> str:
-    """Digest of the library's sources (every file under csrc/)."""
+    """Digest of the library's sources: every file under csrc/ and the C ABI
+    header, whose constants the kernels are compiled with."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "global_l2_norm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+    files = [os.path.join(d, f) for f in sorted(os.listdir(d))]
+    files.append(os.path.join(ROOT, "include", "gclip.h"))
+    for path in files:
+        with open(path, "rb") as fh:
+            h.update(os.path.basename(path).encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
