@@ -118,6 +118,7 @@ gclip::NormArgs norm_args(gclip_handle* h, int32_t grid, float max_norm, float i
   a.out_flag = out_flag;
   a.keep_from = h->keep_from;
   a.resident = h->total_bytes <= h->l2_bytes / 2 ? 1 : 0;
+  a.prefetch = !a.resident && h->total_bytes <= 4 * h->l2_bytes ? 1 : 0;
   return a;
 }
 

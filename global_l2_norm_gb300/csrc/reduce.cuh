@@ -297,6 +297,14 @@ __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max
 // The norm pass of the handle-based clip, shared by the register-engine
 // variants (split, split_wave, single launch).
 //
+// Sets between half of L2 and four times L2 are also prefetched a chunk
+// ahead into L2 (one bulk request per chunk, at normal priority, where the
+// loads themselves ask for evict_first).  Measured on GB300: 120M fp32 clip
+// -0.6 us, fp16 / bf16 sets -3 us, a skipped fp16 clip +0.7 us; most likely
+// the prefetched lines of the last chunks are still in L2 when the scaling
+// pass, which visits them first, starts.  On a 4.9 GB set the extra requests
+// cost 1%, so larger sets are not prefetched.  The arithmetic is unchanged.
+//
 // A grid of G blocks (G fixed per handle: the co-resident count of the
 // single-launch kernel, at most the number of chunks).  Block b takes chunks
 // b, b + G, b + 2G, ...; each of its threads keeps one float-float
@@ -320,6 +328,7 @@ struct NormArgs {
   int32_t* out_flag;
   int64_t keep_from;      // chunks from here on are read with evict_last
   int resident;           // the set fits in half of L2: the rest is read with evict_normal
+  int prefetch;           // each block asks L2 for its next chunk ahead of its loads
 };
 
 __device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
@@ -330,6 +339,16 @@ __device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
   FF acc = {0.f, 0.f};
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const clip_chunk_t ch = a.chunks[c];
+    if (a.prefetch && threadIdx.x == 0 && c + gridDim.x < a.n_chunks) {
+      // One bulk request for the aligned body of this block's next chunk.
+      const clip_chunk_t nx = a.chunks[c + gridDim.x];
+      const uint32_t es = (nx.meta & 0xffu) == GCLIP_F32 ? 4u : 2u;
+      const uint32_t head = min(nx.numel, static_cast<uint32_t>(((16u - (nx.addr & 15u)) & 15u) / es));
+      const uint32_t bytes = (nx.numel - head) / (16u / es) * 16u;
+      if (bytes)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nx.addr + head * es), "r"(bytes)
+                     : "memory");
+    }
     acc = chunk_accumulate<HintMem>(acc, ch, a.inv_scale, c >= a.keep_from ? pol_last : pol_first);
   }
   return block_reduce(acc, red);
