@@ -299,7 +299,11 @@ __global__ void __launch_bounds__(kThreads, 5) k_grad_norm_accumulate(const Norm
   __shared__ int s_flag;
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const uint64_t pol_first = policy_evict_first();
+  // The gradients' lines (read, then overwritten with the sums) at normal
+  // priority for sets up to four times L2: the scaling pass, which starts from
+  // the chunks written last, then finds part of them in L2 (measured: 120M
+  // fp32 -4.5 us, fp16 -4.3 us; nothing lost when no scaling pass writes).
+  const uint64_t pol_first = a.prefetch ? policy_evict_normal() : policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
   FF acc = {0.f, 0.f};
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
