@@ -577,6 +577,12 @@ def run_gclip(args):
                 if peak_src == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": k_bytes,
                 "launch_ms": round(k_ms, 5)}
+    if traffic:
+        # The DRAM-level rate of the same launch: the measured DRAM bytes over
+        # the same time.  Algorithmic bytes above DRAM bytes (L2 reuse) are what
+        # lets `frac` exceed 1.
+        roofline["dram_achieved"] = round(traffic / (k_ms / 1e3) / 1e9, 1)
+        roofline["dram_frac"] = round(traffic / (k_ms / 1e3) / 1e9 / peak, 4)
 
     # end to end through the public API with host buffers
     e2e = None
