@@ -374,3 +374,26 @@ def test_twenty_thousand_small_tensors(variant, dt):
     rec = gpu_clip(ts, 10.0, 0.5, variant)
     compare(before, ts, rec, 10.0, 0.5, f"many-{variant}")
     assert rec["decision"] == g.GCLIP_DECISION_CLIP
+
+
+# -- cache hints change timing only ---------------------------------------------------
+
+@pytest.mark.parametrize("name", ["andrea14m", "andrea120m"])
+def test_l2_hints_do_not_change_results(name):
+    """The 14M set is read with the normal L2 policy, the 120M set with
+    evict_first plus the next-chunk prefetch; an evict_last keep region on
+    top changes neither the record nor a single output bit."""
+    gs = make_gradset(name, device=dev())
+    for t in gs.tensors:
+        t.mul_(30.0)                                   # the clip fires on both sets
+    other = [t.clone() for t in gs.tensors]
+    recs = []
+    for ts, keep in ((gs.tensors, 0), (other, 64 << 20)):
+        with g.GradClipper(ts) as c:
+            c.set_l2_keep(keep)
+            c.clip_(1.0, 0.5)
+            r = c.result()
+            recs.append((r["norm"], r["sumsq_hi"], r["sumsq_lo"], r["coef_hi"], r["coef_lo"]))
+    assert recs[0] == recs[1]
+    for a, b in zip(gs.tensors, other):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
