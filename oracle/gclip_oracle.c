@@ -470,7 +470,11 @@ int oracle_clip_to_f32(const oracle_tensor *in, void *const *out,
     for (int32_t t = 0; t < n_tensors; ++t)
         for (int64_t i = 0; i < in[t].numel; ++i) {
             double x = oracle_decode(in[t].data, i, in[t].dtype);
+#if ORACLE_MUTANT == 19
+            oracle_encode(out[t], i, OR_F32, x * inv_scale);  /* mistake: clip factor lost */
+#else
             oracle_encode(out[t], i, OR_F32, clipped_value(x, inv_scale, res->coef));
+#endif
         }
     return 0;
 }
@@ -596,8 +600,17 @@ int oracle_clip_per_tensor(const oracle_tensor *in, const oracle_tensor *out,
                            int32_t n_tensors, double max_norm,
                            double inv_scale, oracle_result *res)
 {
+#if ORACLE_MUTANT == 18
+    /* mistake: the global clip applied to the whole set, its record copied */
+    if (oracle_clip(in, out, n_tensors, max_norm, inv_scale, res) != 0)
+        return -1;
+    for (int32_t t = 1; t < n_tensors; ++t)
+        res[t] = res[0];
+    return 0;
+#else
     for (int32_t t = 0; t < n_tensors; ++t)
         if (oracle_clip(in + t, out + t, 1, max_norm, inv_scale, res + t) != 0)
             return -1;
     return 0;
+#endif
 }

@@ -28,6 +28,8 @@ MUTANTS = {
     15: "AdamW second moment with beta1",
     16: "accumulation subtracts the last microbatch",
     17: "each contribution clipped before it is added",
+    18: "per-tensor clipping applies the global clip",
+    19: "the fp32 output loses the clip factor",
 }
 
 
