@@ -47,7 +47,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["gclip", "reference"], default="gclip")
     p.add_argument("--variant", choices=["split", "persistent", "split_tma", "persistent_tma", "split_wave"],
                    default="split")
-    p.add_argument("--workload", default="andrea120m")
+    p.add_argument("--workload", default="andrea120m",
+                   help="tiny, andrea14m, andrea120m (default), andrea120m_noclip, andrea120m_fp16, "
+                        "andrea120m_fp16_inf, andrea120m_bf16, andrea1p2b")
     p.add_argument("--pool", type=int, default=32, help="distinct gradient sets per timed run")
     p.add_argument("--l2-keep-mb", type=float, default=None,
                    help="MB of the norm pass kept in L2 for the scaling pass "
