@@ -45,12 +45,15 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=3200)
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["gclip", "reference"], default="gclip")
-    p.add_argument("--variant", choices=["split", "persistent", "split_tma", "persistent_tma", "split_wave"],
+    p.add_argument("--variant", choices=["split", "persistent", "split_tma", "persistent_tma", "split_wave",
+                                         "three_kernel"],
                    default="split")
     p.add_argument("--workload", default="andrea120m",
                    help="tiny, andrea14m, andrea120m (default), andrea120m_noclip, andrea120m_fp16, "
                         "andrea120m_fp16_inf, andrea120m_bf16, andrea1p2b")
-    p.add_argument("--pool", type=int, default=32, help="distinct gradient sets per timed run")
+    p.add_argument("--pool", type=int, default=32,
+                   help="distinct gradient sets per timed run (at most steps / 4, so that "
+                        "every run gives at least four timed runs)")
     p.add_argument("--l2-keep-mb", type=float, default=None,
                    help="MB of the norm pass kept in L2 for the scaling pass "
                         "(default: the library's choice)")
@@ -84,6 +87,12 @@ def algorithmic_bytes(numel: int, elem_bytes: int, decision: str) -> int:
     if decision == "write":
         return 3 * numel * elem_bytes
     return numel * elem_bytes
+
+
+def pool_size(pool: int, steps: int) -> int:
+    """Distinct sets per timed run: at most steps / 4, so that a short run
+    still gives four or more timed runs (and a real p10 / p50 / p90)."""
+    return max(1, min(pool, steps // 4))
 
 
 def rank_env():
@@ -384,7 +393,7 @@ def run_gclip(args):
 
     # one pristine set, P working sets
     pristine = make_gradset(w, device=dev, flat=True)
-    P = 1 if args.warm else max(1, min(args.pool, args.steps))
+    P = 1 if args.warm else pool_size(args.pool, args.steps)
     sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
     clippers = [g.GradClipper(s.tensors, variant=args.variant) for s in sets]
     if args.to_f32:
@@ -528,7 +537,8 @@ def run_gclip(args):
     step_us = sorted(t / n * 1e3 for t, n in runs)
 
     # per-kernel durations for the roofline (events between the launches)
-    launches_per_step = 3 if args.per_tensor else (
+    launches_per_step = 3 if args.per_tensor or (
+        args.variant == "three_kernel" and not (args.to_f32 or args.accumulate)) else (
         2 if args.to_f32 or args.accumulate or not args.variant.startswith("persistent") else 1)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in evs:           # torch creates the CUDA event on its first record
@@ -556,6 +566,11 @@ def run_gclip(args):
         k_bytes, k_ms = nbytes, seg_ms[2]
         # the timed region is back-to-back launches of this one kernel
         k_ms = per_step_ms
+    elif args.variant == "three_kernel":
+        shares = {"k_chunk_sums": (seg_ms[0], w.numel * w.elem_bytes),
+                  "k_grad_scale": (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
+        kernel = max(shares, key=lambda k: shares[k][0])
+        k_ms, k_bytes = shares[kernel]
     else:
         tma = args.variant.endswith("tma")
         shares = {("k_norm_tma" if tma else "k_grad_norm_partial"): (seg_ms[0], w.numel * w.elem_bytes),
@@ -635,6 +650,10 @@ def run_gclip(args):
                "d2h_bytes_per_step": norm_h.element_size() + flag_h.element_size(),
                "ms_per_step": round(e2e_ms, 4),
                "steps": n_e2e,
+               "d2h": "the norm and the nonfinite flag (8 B); the clipped gradients stay "
+                      "in device memory, where the optimizer step reads them",
+               "bound": "the host-to-device copy of the 369 MB set from pinned memory; "
+                        "the clip itself overlaps it",
                "pipelining": "the H2D copy of step k+1 (copy stream) overlaps the clip of step k"}
 
     cpu = cpu_all = None
@@ -680,9 +699,15 @@ def run_gclip(args):
             "elements_per_s": round(w.numel * args.steps * world / (total_ms / 1e3), 1),
             "us_per_step_p10_p50_p90": [round(step_us[int(q * (len(step_us) - 1))], 2)
                                          for q in (0.1, 0.5, 0.9)],
-            "kernel_ms": {"norm": round(seg_ms[0], 5), "scale": round(seg_ms[2], 5)}
-            if args.variant.startswith("split")
-            else {"persistent": round(seg_ms[2], 5)},
+            "kernel_ms": ({"norm": round(seg_ms[0], 5), "scale": round(seg_ms[2], 5)}
+                          if args.variant.startswith("split") else
+                          {"chunk_sums": round(seg_ms[0], 5), "final": round(seg_ms[1], 5),
+                           "scale": round(seg_ms[2], 5)}
+                          if args.variant == "three_kernel" else
+                          {"persistent": round(seg_ms[2], 5)}),
+            "kernel_ms_note": "each launch alone between events (no programmatic dependent "
+                              "launch), the L2 not flushed between clips; a norm pass that "
+                              "follows a writing clip also absorbs that clip's write-backs",
             "roofline": roofline,
             "clocks": clocks,
             "e2e": e2e,
@@ -709,7 +734,7 @@ def run_adamw(args):
     g.build()
     w = WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(dev)
-    P = max(1, min(args.pool, args.steps))
+    P = pool_size(args.pool, args.steps)
     pristine = make_gradset(w, device=dev, flat=True)
     sets = [make_gradset(w, device=dev, flat=True) for _ in range(P)]
     states = []
@@ -754,29 +779,69 @@ def run_adamw(args):
     timed(fused, args.warmup, lambda: None)
     fused_ms = timed(fused, args.steps, lambda: None)
 
-    # unfused: clip (rewrites the gradients), then torch's fused AdamW
+    # unfused: clip (rewrites the gradients), then torch's fused AdamW.  Both
+    # pipelines are also captured as one CUDA graph per timed run and
+    # replayed, so that the comparison is between kernels, without the
+    # optimizer's host-side work.
     params = [[torch.nn.Parameter(st[0].view(t.shape)) for st, t in zip(states[i], sets[i].tensors)]
               for i in range(P)]
     for i in range(P):
         for prm, t in zip(params[i], sets[i].tensors):
             prm.grad = t if t.dtype == torch.float32 else None
     have_torch = all(p_.grad is not None for ps in params for p_ in ps)
-    unfused_ms = None
+    unfused_ms = unfused_graph_ms = fused_graph_ms = None
+
+    def restore_grads():
+        for s_ in sets:
+            s_.flat.copy_(pristine.flat)
+
+    def graph_of(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):      # warm-up on a side stream, as capture wants
+            for i in range(P):
+                fn(i)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(P):
+                fn(i)
+        torch.cuda.synchronize()
+        return gr
+
+    def timed_graph(gr, steps, restore):
+        total, done = 0.0, 0
+        while done < steps:
+            restore()
+            flush.fill_(1)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+            done += P
+        return total / done
+
+    fused_graph = graph_of(lambda i: clippers[i].clip_adamw_(w.max_norm, w.inv_scale, step=7, **hp))
+    timed_graph(fused_graph, args.warmup, lambda: None)
+    fused_graph_ms = timed_graph(fused_graph, args.steps, lambda: None)
+    del fused_graph
     if have_torch:
-        opts = [torch.optim.AdamW(ps, fused=True, **{k: v for k, v in hp.items()
-                                                     if k not in ("beta1", "beta2")},
+        opts = [torch.optim.AdamW(ps, fused=True, capturable=True,
+                                  **{k: v for k, v in hp.items() if k not in ("beta1", "beta2")},
                                   betas=(hp["beta1"], hp["beta2"])) for ps in params]
 
         def unfused(i):
             clippers[i].clip_(w.max_norm, w.inv_scale)
             opts[i].step()
 
-        def restore_grads():
-            for s in sets:
-                s.flat.copy_(pristine.flat)
-
         timed(unfused, args.warmup, restore_grads)
         unfused_ms = timed(unfused, args.steps, restore_grads)
+        unfused_graph = graph_of(unfused)
+        timed_graph(unfused_graph, args.warmup, restore_grads)
+        unfused_graph_ms = timed_graph(unfused_graph, args.steps, restore_grads)
+        del unfused_graph
 
     es = w.elem_bytes
     fused_bytes = w.numel * (2 * es + 24)        # g read twice; w, m, v read and written
@@ -800,11 +865,17 @@ def run_adamw(args):
                    "l2": "pool of distinct sets, L2 flushed before each timed run"},
         "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(value / peak, 4)},
+        "fused_graph_ms_per_step": round(fused_graph_ms, 5),
         "unfused": None if unfused_ms is None else {
-            "what": "clip_grad_norm (split) then torch.optim.AdamW(fused=True); the time "
-                    "includes torch's host-side optimizer overhead",
-            "ms_per_step": round(unfused_ms, 5), "bytes_per_step": unfused_bytes,
-            "speedup_of_fused": round(unfused_ms / fused_ms, 3)},
+            "what": "clip_grad_norm (split) then torch.optim.AdamW(fused=True, capturable=True)",
+            "ms_per_step": round(unfused_ms, 5),
+            "ms_per_step_note": "eager: includes torch's host-side optimizer work",
+            "graph_ms_per_step": round(unfused_graph_ms, 5),
+            "graph_note": "both pipelines captured as one CUDA graph per timed run and "
+                          "replayed: kernel time only",
+            "bytes_per_step": unfused_bytes,
+            "speedup_of_fused": round(unfused_ms / fused_ms, 3),
+            "speedup_of_fused_graphs": round(unfused_graph_ms / fused_graph_ms, 3)},
     }
     for c in clippers:
         c.close()

@@ -37,7 +37,8 @@ VARIANTS = {"split": GCLIP_VARIANT_SPLIT,
             "persistent": GCLIP_VARIANT_PERSISTENT,
             "split_tma": _abi.GCLIP_VARIANT_SPLIT_TMA,
             "persistent_tma": _abi.GCLIP_VARIANT_PERSISTENT_TMA,
-            "split_wave": _abi.GCLIP_VARIANT_SPLIT_WAVE}
+            "split_wave": _abi.GCLIP_VARIANT_SPLIT_WAVE,
+            "three_kernel": _abi.GCLIP_VARIANT_THREE_KERNEL}
 
 
 def build(force: bool = False) -> str:
@@ -236,6 +237,17 @@ class GradClipper:
         check("clip_read_result", self._lib.clip_read_result(
             self._h, ctypes.byref(r), _stream_handle(stream, self.device)))
         return {k: getattr(r, k) for k, _ in clip_result_t._fields_ if k != "reserved"}
+
+    def last_status(self, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Enqueue a copy of the record's status word (GCLIP_STATUS_*) into
+        the device int32 tensor `out` (a new one if None); no sync."""
+        if out is None:
+            out = torch.empty(1, dtype=torch.int32, device=self.device)
+        if out.dtype != torch.int32 or out.device != self.device:
+            raise ValueError("out must be an int32 tensor on the gradients' device")
+        check("clip_last_status", self._lib.clip_last_status(
+            self._h, out.data_ptr(), _stream_handle(stream, self.device)))
+        return out
 
     def reset(self, stream=None) -> None:
         check("clip_reset", self._lib.clip_reset(self._h, _stream_handle(stream, self.device)))

@@ -34,11 +34,12 @@ GCLIP_VARIANT_PERSISTENT = 1
 GCLIP_VARIANT_SPLIT_TMA = 2
 GCLIP_VARIANT_PERSISTENT_TMA = 3
 GCLIP_VARIANT_SPLIT_WAVE = 4
+GCLIP_VARIANT_THREE_KERNEL = 5
 
 GCLIP_CHUNK_BYTES = 32768
 GCLIP_MAX_TENSORS = 1 << 24
 GCLIP_NOALLOC_MAX_CHUNKS = 65536
-GCLIP_NOALLOC_SCRATCH_BYTES = GCLIP_NOALLOC_MAX_CHUNKS * 8 + 256
+GCLIP_NOALLOC_SCRATCH_BYTES = GCLIP_NOALLOC_MAX_CHUNKS * 16 + 256
 
 
 class clip_tensor_desc_t(ctypes.Structure):
@@ -82,6 +83,7 @@ _SIGNATURES = {
     "clip_result_device": (_P, [_P]),
     "clip_read_result": (ctypes.c_int, [_P, ctypes.POINTER(clip_result_t), _P]),
     "clip_reset": (ctypes.c_int, [_P, _P]),
+    "clip_last_status": (ctypes.c_int, [_P, _P, _P]),
     "clip_num_chunks": (ctypes.c_int64, [_P]),
     "clip_persistent_grid": (ctypes.c_int32, [_P]),
     "clip_tma_grid": (ctypes.c_int32, [_P]),

@@ -17,7 +17,8 @@ namespace gclip {
 
 constexpr int kThreads = 256;             // threads per block, every kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 8;                // 16-byte vectors in flight per thread
+constexpr int kUnroll = 8;                // 16-byte vectors in flight per thread (scaling)
+constexpr int kNormUnroll = 8;            // the same in the norm pass
 constexpr long long kDefaultTimeoutNs = 1000000000LL;  // grid barrier: 1 s
 
 struct SyncWords {
@@ -62,6 +63,29 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
 }
 
 // ---------------------------------------------------------------------------
+// The sum of squares in two bins.  A square is taken in fp32, so an unscaled
+// element y = x * inv_scale with |y| < 2^-63 has a subnormal or zero square.
+// A vector (or scalar element) whose fp32 sum of squares is at least kTinySq
+// goes to `big`; the others go to `tiny` as the squares of x * inv_scale *
+// 2^K, with K chosen per call so that inv_scale * 2^K is a finite fp32 number
+// (K = 96 unless inv_scale > 2^30).  Both bins are float-float sums; the
+// total is big + tiny * 2^-2K, formed in double by the final reduction.  A
+// vector in `tiny` has every |y| < 2^-50, so its scaled squares are below
+// 2^92 (no overflow over 2^35 vectors), and every |y| >= 2^(-63-K) (2^-159)
+// has a normal scaled square: neither bin underflows where it matters.
+
+constexpr float kTinySq = 0x1p-100f;
+constexpr int kTinyExpMax = 96;
+
+struct SumSq {
+  FF big, tiny;
+};
+
+__device__ __forceinline__ SumSq sumsq_add(SumSq a, SumSq b) {
+  return SumSq{ff_add(a.big, b.big), ff_add(a.tiny, b.tiny)};
+}
+
+// ---------------------------------------------------------------------------
 // Element formats.  A 16-byte vector holds 4 fp32 or 8 fp16/bf16 elements,
 // element 0 in the lowest bytes.
 
@@ -78,13 +102,13 @@ struct Fmt<GCLIP_F32> {
   __device__ static __forceinline__ void store1(uint64_t a, float v) {
     *reinterpret_cast<float*>(a) = v;
   }
-  // Sum of the four squares, one rounding per element (the first product,
-  // then fused multiply-adds in element order).
-  __device__ static __forceinline__ float sumsq(uint4 v, float s) {
-    const float y0 = __fmul_rn(__uint_as_float(v.x), s);
-    const float y1 = __fmul_rn(__uint_as_float(v.y), s);
-    const float y2 = __fmul_rn(__uint_as_float(v.z), s);
-    const float y3 = __fmul_rn(__uint_as_float(v.w), s);
+  // Sum of the four squares of x * k, one rounding per element (the first
+  // product, then fused multiply-adds in element order).
+  __device__ static __forceinline__ float sumsq(uint4 v, float k) {
+    const float y0 = __fmul_rn(__uint_as_float(v.x), k);
+    const float y1 = __fmul_rn(__uint_as_float(v.y), k);
+    const float y2 = __fmul_rn(__uint_as_float(v.z), k);
+    const float y3 = __fmul_rn(__uint_as_float(v.w), k);
     float r = __fmul_rn(y0, y0);
     r = __fmaf_rn(y1, y1, r);
     r = __fmaf_rn(y2, y2, r);
@@ -136,11 +160,12 @@ struct Fmt<GCLIP_F16> {
   __device__ static __forceinline__ void store1(uint64_t a, float v) {
     *reinterpret_cast<unsigned short*>(a) = __half_as_ushort(__float2half_rn(v));
   }
-  __device__ static __forceinline__ float sumsq(uint4 v, float s) {
+  // Sum of the eight squares of x * k, as for fp32.
+  __device__ static __forceinline__ float sumsq(uint4 v, float k) {
     const float2 a = widen(v.x), b = widen(v.y), c = widen(v.z), d = widen(v.w);
-    const float y[8] = {__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(b.x, s),
-                        __fmul_rn(b.y, s), __fmul_rn(c.x, s), __fmul_rn(c.y, s),
-                        __fmul_rn(d.x, s), __fmul_rn(d.y, s)};
+    const float y[8] = {__fmul_rn(a.x, k), __fmul_rn(a.y, k), __fmul_rn(b.x, k),
+                        __fmul_rn(b.y, k), __fmul_rn(c.x, k), __fmul_rn(c.y, k),
+                        __fmul_rn(d.x, k), __fmul_rn(d.y, k)};
     float r = __fmul_rn(y[0], y[0]);
 #pragma unroll
     for (int i = 1; i < 8; ++i) r = __fmaf_rn(y[i], y[i], r);
@@ -192,11 +217,12 @@ struct Fmt<GCLIP_BF16> {
   __device__ static __forceinline__ void store1(uint64_t a, float v) {
     *reinterpret_cast<__nv_bfloat16*>(a) = __float2bfloat16_rn(v);
   }
-  __device__ static __forceinline__ float sumsq(uint4 v, float s) {
+  // Sum of the eight squares of x * k, as for fp32.
+  __device__ static __forceinline__ float sumsq(uint4 v, float k) {
     const float2 a = widen(v.x), b = widen(v.y), c = widen(v.z), d = widen(v.w);
-    const float y[8] = {__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(b.x, s),
-                        __fmul_rn(b.y, s), __fmul_rn(c.x, s), __fmul_rn(c.y, s),
-                        __fmul_rn(d.x, s), __fmul_rn(d.y, s)};
+    const float y[8] = {__fmul_rn(a.x, k), __fmul_rn(a.y, k), __fmul_rn(b.x, k),
+                        __fmul_rn(b.y, k), __fmul_rn(c.x, k), __fmul_rn(c.y, k),
+                        __fmul_rn(d.x, k), __fmul_rn(d.y, k)};
     float r = __fmul_rn(y[0], y[0]);
 #pragma unroll
     for (int i = 1; i < 8; ++i) r = __fmaf_rn(y[i], y[i], r);
@@ -226,6 +252,23 @@ struct Fmt<GCLIP_BF16> {
     return __bfloat162float(__float2bfloat16_rn(v));
   }
 };
+
+// The elements of one 16-byte vector widened to fp32, element 0 first
+// (4 for fp32, 8 for fp16/bf16).
+template <int DT>
+__device__ __forceinline__ void widen_vec(uint4 g, float (&x)[8]) {
+  if constexpr (DT == GCLIP_F32) {
+    x[0] = __uint_as_float(g.x);
+    x[1] = __uint_as_float(g.y);
+    x[2] = __uint_as_float(g.z);
+    x[3] = __uint_as_float(g.w);
+  } else {
+    const float2 a = Fmt<DT>::widen(g.x), b = Fmt<DT>::widen(g.y), c = Fmt<DT>::widen(g.z),
+                 d = Fmt<DT>::widen(g.w);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+  }
+}
 
 // How one chunk is laid out for vector access: `head` scalar elements up to
 // the first 16-byte boundary, `nvec` aligned vectors, then `ntail` scalars.

@@ -52,14 +52,16 @@ struct gclip_handle {
   int64_t keep_from;         // first chunk the norm pass reads with evict_last
   int64_t l2_bytes;          // L2 size of the device
   int32_t variant;
-  int32_t grid_persistent;   // blocks of the register engine (co-resident)
+  int32_t grid_persistent;   // blocks of the register engine's norm pass (co-resident)
+  int32_t grid_wave;         // blocks of a scaling wave (co-resident)
   int32_t grid_tma;          // blocks of the TMA engine (co-resident)
   int32_t coop;
   int32_t debug_extra;
   long long timeout_ns;
   void* arena;
   clip_chunk_t* d_chunks;
-  float2* d_partials;        // one entry per block of the norm pass (G)
+  float4* d_partials;        // one two-bin sum per chunk (per-chunk kernels) or per
+                             // block of the norm pass (G <= chunks)
   clip_result_t* d_result;
   SyncWords* d_sync;
   int64_t* d_first;          // first chunk of each tensor, n_tensors + 1 entries
@@ -95,6 +97,32 @@ struct DeviceGuard {
 
 bool valid_scalar(float v) { return std::isfinite(v) && v > 0.0f; }
 
+// The tiny bin's multiplier inv_scale * 2^K and K: K = kTinyExpMax unless
+// that product would exceed 2^126 (exact: a power-of-two scaling).
+struct TinyScale {
+  float st;
+  int k;
+};
+
+TinyScale tiny_scale(float inv_scale) {
+  int k = gclip::kTinyExpMax;
+  double st = std::ldexp(static_cast<double>(inv_scale), k);
+  while (k > 0 && st > 0x1p126) {
+    --k;
+    st *= 0.5;
+  }
+  return TinyScale{static_cast<float>(st), k};
+}
+
+// Blocks of a grid that strides over n chunks with at most `resident`
+// blocks: the fewest that keep the largest share ceil(n / resident), so
+// that every block gets the same number of chunks or one less.
+int32_t balanced_grid(int64_t resident, int64_t n) {
+  if (resident <= 0 || n <= 0) return static_cast<int32_t>(resident < n ? resident : n);
+  const int64_t per = (n + resident - 1) / resident;
+  return static_cast<int32_t>((n + per - 1) / per);
+}
+
 // The norm pass marks its last `bytes` (rounded to whole chunks) evict_last
 // in L2, for the scaling pass to find there.
 void set_keep(gclip_handle* h, int64_t bytes) {
@@ -113,6 +141,9 @@ gclip::NormArgs norm_args(gclip_handle* h, int32_t grid, float max_norm, float i
   a.expected = static_cast<unsigned int>(grid) + extra;
   a.max_norm = max_norm;
   a.inv_scale = inv_scale;
+  const TinyScale ts = tiny_scale(inv_scale);
+  a.inv_scale_tiny = ts.st;
+  a.tiny_exp = ts.k;
   a.res = h->d_result;
   a.out_norm = out_norm;
   a.out_flag = out_flag;
@@ -163,7 +194,7 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   // it is at most the number of chunks, so size the block sums for that.
   const size_t off_chunks = 0;
   const size_t off_partials = round_up(off_chunks + n * sizeof(clip_chunk_t), 256);
-  const size_t off_result = round_up(off_partials + n * sizeof(float2), 256);
+  const size_t off_result = round_up(off_partials + n * sizeof(float4), 256);
   const size_t off_sync = round_up(off_result + sizeof(clip_result_t), 256);
   const size_t nt = static_cast<size_t>(n_tensors);
   const size_t off_first = round_up(off_sync + sizeof(SyncWords), 256);
@@ -188,7 +219,7 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   }
   char* base = static_cast<char*>(h->arena);
   h->d_chunks = reinterpret_cast<clip_chunk_t*>(base + off_chunks);
-  h->d_partials = reinterpret_cast<float2*>(base + off_partials);
+  h->d_partials = reinterpret_cast<float4*>(base + off_partials);
   h->d_result = reinterpret_cast<clip_result_t*>(base + off_result);
   h->d_sync = reinterpret_cast<SyncWords*>(base + off_sync);
   h->d_first = reinterpret_cast<int64_t*>(base + off_first);
@@ -208,7 +239,10 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gclip::k_clip_persistent,
                                                       gclip::kThreads, 0);
-  int per_sm_tma = 0;
+  int per_sm_tma = 0, per_sm_wave = 0;
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_wave, gclip::k_grad_scale_wave,
+                                                      gclip::kThreads, 0);
   for (const void* fn : {reinterpret_cast<const void*>(gclip::k_norm_tma),
                          reinterpret_cast<const void*>(gclip::k_scale_tma),
                          reinterpret_cast<const void*>(gclip::k_clip_persistent_tma)})
@@ -227,10 +261,10 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   }
   h->l2_bytes = l2;
   set_keep(h, 0);
-  const int64_t resident = static_cast<int64_t>(sms) * per_sm;
-  h->grid_persistent = static_cast<int32_t>(resident < h->n_chunks ? resident : h->n_chunks);
-  const int64_t resident_tma = static_cast<int64_t>(sms) * per_sm_tma;
-  h->grid_tma = static_cast<int32_t>(resident_tma < h->n_chunks ? resident_tma : h->n_chunks);
+  h->grid_persistent = balanced_grid(static_cast<int64_t>(sms) * per_sm, h->n_chunks);
+  h->grid_tma = balanced_grid(static_cast<int64_t>(sms) * per_sm_tma, h->n_chunks);
+  const int64_t wave = static_cast<int64_t>(sms) * per_sm_wave;
+  h->grid_wave = static_cast<int32_t>(wave < h->n_chunks ? wave : h->n_chunks);
   h->coop = coop;
   *out = h;
   return GCLIP_OK;
@@ -248,11 +282,22 @@ cudaError_t launch_scale(clip_handle_t h, cudaStream_t s, bool pdl) {
     unsigned int* work = &h->d_sync->work;
     void* args[] = {&chunks, &nc, &cres, &work};
     return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale_wave),
-                      static_cast<unsigned int>(h->grid_persistent), s, args, pdl);
+                      static_cast<unsigned int>(h->grid_wave), s, args, pdl);
   }
-  void* args[] = {&chunks, &nc, &cres};
-  return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale),
+  gclip::TableChunks src{chunks};
+  void* args[] = {&src, &nc, &cres};
+  return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale<gclip::TableChunks>),
                     static_cast<unsigned int>(nc), s, args, pdl);
+}
+
+// The final reduction alone, for a set with no chunks (norm 0, PASS).
+cudaError_t launch_empty(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
+                         int32_t* out_flag, cudaStream_t s) {
+  const float4* partials = h->d_partials;
+  int64_t n = 0;
+  int k = tiny_scale(inv_scale).k;
+  void* args[] = {&partials, &n, &max_norm, &inv_scale, &k, &h->d_result, &out_norm, &out_flag};
+  return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, args, false);
 }
 
 // Enqueue one clip.  `events` (may be NULL) are recorded between the steps;
@@ -260,7 +305,7 @@ cudaError_t launch_scale(clip_handle_t h, cudaStream_t s, bool pdl) {
 int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
             int32_t* out_flag, cudaStream_t s, cudaEvent_t const* events) {
   int64_t nc = h->n_chunks;
-  const float2* partials = h->d_partials;
+  const float4* partials = h->d_partials;
   const bool pdl = events == nullptr;
   cudaError_t e = cudaSuccess;
   auto mark = [&](int i) {
@@ -271,9 +316,27 @@ int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
   if (nc == 0) {
     mark(1);
     mark(2);
-    void* args[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm, &out_flag};
+    if (e == cudaSuccess) e = launch_empty(h, max_norm, inv_scale, out_norm, out_flag, s);
+  } else if (h->variant == GCLIP_VARIANT_THREE_KERNEL) {
+    // The clipping page's pipeline as written: per-chunk sums, one block that
+    // reduces them and decides, one block per chunk that scales.
+    const TinyScale ts = tiny_scale(inv_scale);
+    gclip::TableChunks src{h->d_chunks};
+    float4* parts = h->d_partials;
+    unsigned int* no_clear = nullptr;
+    int resident = h->total_bytes <= h->l2_bytes / 2 ? 1 : 0;
+    float st = ts.st;
+    int k = ts.k;
+    void* a1[] = {&src, &inv_scale, &st, &parts, &no_clear, &resident};
     if (e == cudaSuccess)
-      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, args, false);
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_chunk_sums<gclip::TableChunks>),
+                     static_cast<unsigned int>(nc), s, a1, pdl);
+    mark(1);
+    void* a2[] = {&partials, &nc, &max_norm, &inv_scale, &k, &h->d_result, &out_norm, &out_flag};
+    if (e == cudaSuccess)
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a2, pdl);
+    mark(2);
+    if (e == cudaSuccess) e = launch_scale(h, s, pdl);
   } else if (h->variant == GCLIP_VARIANT_SPLIT || h->variant == GCLIP_VARIANT_SPLIT_WAVE) {
     gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag, 0);
     void* a1[] = {&a};
@@ -382,7 +445,7 @@ extern "C" int clip_destroy(clip_handle_t h) {
 
 extern "C" int clip_set_variant(clip_handle_t h, int32_t variant) {
   if (h == nullptr) return GCLIP_ERR_INVALID_ARG;
-  if (variant < GCLIP_VARIANT_SPLIT || variant > GCLIP_VARIANT_SPLIT_WAVE)
+  if (variant < GCLIP_VARIANT_SPLIT || variant > GCLIP_VARIANT_THREE_KERNEL)
     return GCLIP_ERR_INVALID_ARG;
   const bool coop = variant == GCLIP_VARIANT_PERSISTENT || variant == GCLIP_VARIANT_PERSISTENT_TMA;
   const int32_t grid = (variant == GCLIP_VARIANT_SPLIT_TMA || variant == GCLIP_VARIANT_PERSISTENT_TMA)
@@ -406,6 +469,19 @@ extern "C" int clip_read_result(clip_handle_t h, clip_result_t* out, void* strea
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(out, h->d_result, sizeof(clip_result_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  return GCLIP_OK;
+}
+
+extern "C" int clip_last_status(clip_handle_t h, int32_t* d_out, void* stream) {
+  if (h == nullptr || d_out == nullptr) return GCLIP_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  const cudaError_t e = cudaMemcpyAsync(d_out, &h->d_result->status, sizeof(int32_t),
+                                        cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GCLIP_ERR_CUDA;
@@ -506,9 +582,7 @@ int enqueue_norm_then(clip_handle_t h, float max_norm, float inv_scale, float* o
   int64_t nc = h->n_chunks;
   cudaError_t e = cudaSuccess;
   if (nc == 0) {
-    const float2* partials = h->d_partials;
-    void* a[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm, &out_flag};
-    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a, false);
+    e = launch_empty(h, max_norm, inv_scale, out_norm, out_flag, s);
   } else {
     gclip::NormArgs a = norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_flag, 0);
     void* a1[] = {&a};
@@ -560,10 +634,7 @@ extern "C" int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float 
   int64_t nc = h->n_chunks;
   cudaError_t e = cudaSuccess;
   if (nc == 0) {
-    const float2* partials = h->d_partials;
-    void* a[] = {&partials, &nc, &max_norm, &inv_scale, &h->d_result, &out_norm,
-                 &out_nonfinite_flag};
-    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a, false);
+    e = launch_empty(h, max_norm, inv_scale, out_norm, out_nonfinite_flag, s);
   } else {
     gclip::NormArgs a =
         norm_args(h, h->grid_persistent, max_norm, inv_scale, out_norm, out_nonfinite_flag, 0);
@@ -642,8 +713,8 @@ extern "C" int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int64_t nc = h->n_chunks;
   const clip_chunk_t* chunks = h->d_chunks;
-  float2* partials = h->d_partials;
-  const float2* cpartials = partials;
+  float4* partials = h->d_partials;
+  const float4* cpartials = partials;
   const int64_t* first = h->d_first;
   clip_result_t* recs = h->d_trec;
   const clip_result_t* crecs = recs;
@@ -651,21 +722,26 @@ extern "C" int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float 
   const int64_t* cwlist = wlist;
   unsigned int* wcount = h->d_wcount;
   cudaError_t e = cudaSuccess;
+  const TinyScale ts = tiny_scale(inv_scale);
+  float st = ts.st;
+  int k = ts.k;
   if (nc > 0) {
     // Not a programmatic dependent: it empties the write list, which the
     // previous call's scaling kernel reads until it ends.
-    void* a1[] = {&chunks, &inv_scale, &partials, &wcount};
-    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_chunk_partials),
+    gclip::TableChunks src{chunks};
+    int resident = 0;
+    void* a1[] = {&src, &inv_scale, &st, &partials, &wcount, &resident};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_chunk_sums<gclip::TableChunks>),
                    static_cast<unsigned int>(nc), s, a1, false);
   }
-  void* a2[] = {&cpartials, &first, &max_norm, &inv_scale, &recs,
+  void* a2[] = {&cpartials, &first, &max_norm, &inv_scale, &k, &recs,
                 &out_norms, &out_nonfinite_flags, &wlist, &wcount};
   if (e == cudaSuccess)
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_tensor_final), nt, s, a2, nc > 0);
   void* a3[] = {&chunks, &cwlist, &wcount, &crecs};
   if (e == cudaSuccess && nc > 0)
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_scale_per_tensor),
-                   static_cast<unsigned int>(h->grid_persistent), s, a3, true);
+                   static_cast<unsigned int>(h->grid_wave), s, a3, true);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GCLIP_ERR_CUDA;
@@ -694,75 +770,48 @@ extern "C" int clip_read_per_tensor(clip_handle_t h, clip_result_t* out, int32_t
 
 namespace gclip {
 
-// The scratch of clip_grad_norm_flat_noalloc: the per-chunk partial sums,
-// then the result record.  Compiled into the library, so it costs every GPU
-// that loads the library GCLIP_NOALLOC_SCRATCH_BYTES until exit.
-constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(GCLIP_NOALLOC_MAX_CHUNKS) * 8;
+// The scratch of clip_grad_norm_flat_noalloc: one two-bin partial sum per
+// chunk, then the result record.  Compiled into the library, so it costs
+// every GPU that loads the library GCLIP_NOALLOC_SCRATCH_BYTES until exit.
+constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(GCLIP_NOALLOC_MAX_CHUNKS) * sizeof(float4);
 static_assert(kNoAllocPartialBytes + sizeof(clip_result_t) <= GCLIP_NOALLOC_SCRATCH_BYTES,
               "record does not fit the scratch");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GCLIP_NOALLOC_SCRATCH_BYTES];
-
-// Chunk c of a single tensor at `base`, cut exactly as the host planner cuts
-// one tensor: the first chunk takes the elements before the first 16-byte
-// boundary plus a full chunk, every later chunk starts aligned.
-__device__ __forceinline__ clip_chunk_t flat_chunk(uint64_t base, int64_t numel, int32_t dtype,
-                                                   int64_t c) {
-  const int64_t es = dtype == GCLIP_F32 ? 4 : 2;
-  const int64_t per = GCLIP_CHUNK_BYTES / es;
-  const int64_t head = static_cast<int64_t>((16u - (base & 15u)) & 15u) / es;
-  const int64_t start = c == 0 ? 0 : head + c * per;
-  const int64_t want = c == 0 ? head + per : per;
-  const int64_t left = numel - start;
-  clip_chunk_t ch;
-  ch.addr = base + static_cast<uint64_t>(start * es);
-  ch.numel = static_cast<uint32_t>(left < want ? left : want);
-  ch.meta = static_cast<uint32_t>(dtype);
-  return ch;
-}
-
-__global__ void __launch_bounds__(kThreads) k_grad_norm_partial_flat(uint64_t base, int64_t numel,
-                                                                     int32_t dtype, float inv_scale,
-                                                                     float2* __restrict__ partials) {
-  __shared__ FF red[kWarps];
-  asm volatile("griddepcontrol.launch_dependents;");
-  const clip_chunk_t c = flat_chunk(base, numel, dtype, blockIdx.x);
-  const FF acc = chunk_sumsq<PlainMem>(c, inv_scale, red, 0);
-  if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
-}
-
-__global__ void __launch_bounds__(kThreads) k_grad_scale_flat(uint64_t base, int64_t numel,
-                                                              int32_t dtype, int64_t n_chunks,
-                                                              const clip_result_t* res) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int decision = res->decision;
-  const float chi = res->coef_hi, clo = res->coef_lo;
-  if (!must_write(decision, chi, clo)) return;
-  const clip_chunk_t c =
-      flat_chunk(base, numel, dtype, n_chunks - 1 - static_cast<int64_t>(blockIdx.x));
-  chunk_scale<PlainMem>(c, chi, clo, 0);
-}
 
 }  // namespace gclip
 
 namespace {
 
 constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoAllocMaxDevices];  // device address of the scratch, per device
 
-// Device address of the scratch array on `dev` (current), looked up once.
-void* noalloc_scratch(int dev) {
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+// What the entry point needs to know about a device, looked up once.
+struct NoAllocDevice {
+  char* scratch;  // device address of gclip::g_noalloc_scratch on that device
+  int64_t l2;     // L2 size in bytes
+};
+
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+
+// The set-up of device `dev` (the current device): the scratch array's
+// device address and the L2 size, looked up on the first call and kept.
+bool noalloc_device(int dev, NoAllocDevice* out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return false;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  NoAllocDevice& d = g_noalloc[dev];
+  if (d.scratch == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, gclip::g_noalloc_scratch) != cudaSuccess) {
+    int l2 = 0;
+    if (cudaGetSymbolAddress(&p, gclip::g_noalloc_scratch) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
-      return nullptr;
+      return false;
     }
-    g_noalloc_addr[dev] = p;
+    d.l2 = l2;
+    d.scratch = static_cast<char*>(p);
   }
-  return g_noalloc_addr[dev];
+  *out = d;
+  return true;
 }
 
 }  // namespace
@@ -789,30 +838,35 @@ extern "C" int clip_grad_norm_flat_noalloc(void* grads, int64_t numel, int32_t d
     cudaGetLastError();
     return GCLIP_ERR_CUDA;
   }
-  char* scratch = static_cast<char*>(noalloc_scratch(dev));
-  if (scratch == nullptr) return GCLIP_ERR_CUDA;
-  float2* partials = reinterpret_cast<float2*>(scratch);
-  clip_result_t* record = reinterpret_cast<clip_result_t*>(scratch + gclip::kNoAllocPartialBytes);
-  const float2* cpartials = partials;
+  NoAllocDevice d;
+  if (!noalloc_device(dev, &d)) return GCLIP_ERR_CUDA;
+  float4* partials = reinterpret_cast<float4*>(d.scratch);
+  clip_result_t* record = reinterpret_cast<clip_result_t*>(d.scratch + gclip::kNoAllocPartialBytes);
+  const float4* cpartials = partials;
+  const TinyScale ts = tiny_scale(inv_scale);
+  float st = ts.st;
+  int k = ts.k;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
 
-  void* a2[] = {&cpartials, &nc, &max_norm, &inv_scale, &record, &out_norm, &out_nonfinite_flag};
+  // The three launches of GCLIP_VARIANT_THREE_KERNEL, over chunks computed
+  // from the buffer instead of read from a table.
+  void* a2[] = {&cpartials, &nc, &max_norm, &inv_scale, &k, &record, &out_norm, &out_nonfinite_flag};
   if (nc == 0) {
     e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a2, false);
   } else {
-    uint64_t b = base;
-    int64_t n = numel;
-    int32_t dt = dtype;
-    void* a1[] = {&b, &n, &dt, &inv_scale, &partials};
-    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_partial_flat),
+    gclip::FlatChunks src{base, numel, dtype};
+    unsigned int* no_clear = nullptr;
+    int resident = numel * es <= d.l2 / 2 ? 1 : 0;
+    void* a1[] = {&src, &inv_scale, &st, &partials, &no_clear, &resident};
+    e = launch_pdl(reinterpret_cast<const void*>(gclip::k_chunk_sums<gclip::FlatChunks>),
                    static_cast<unsigned int>(nc), s, a1, false);
     if (e == cudaSuccess)
       e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_norm_final), 1, s, a2, true);
     const clip_result_t* crecord = record;
-    void* a3[] = {&b, &n, &dt, &nc, &crecord};
+    void* a3[] = {&src, &nc, &crecord};
     if (e == cudaSuccess)
-      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale_flat),
+      e = launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale<gclip::FlatChunks>),
                      static_cast<unsigned int>(nc), s, a3, true);
   }
   if (e != cudaSuccess) {

@@ -12,8 +12,10 @@ namespace gclip {
 // Split variant: the norm pass (with the final reduction in the last block)
 // and the scaling pass as two launches.
 
-__global__ void __launch_bounds__(kThreads) k_grad_norm_partial(const NormArgs a) {
-  __shared__ FF red[kWarps];
+// Four blocks per SM (up to 64 registers): at five (48 registers) the
+// two-bin sums spill and the clip took 3 us longer (measured, 120M fp32).
+__global__ void __launch_bounds__(kThreads, 4) k_grad_norm_partial(const NormArgs a) {
+  __shared__ SumSq red[kWarps];
   __shared__ int s_flag;
   // Let the dependent scaling launch be scheduled while this grid runs.
   asm volatile("griddepcontrol.launch_dependents;");
@@ -21,24 +23,49 @@ __global__ void __launch_bounds__(kThreads) k_grad_norm_partial(const NormArgs a
   // kernel that produced the gradients): wait for it to finish before
   // reading any gradient.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const FF bsum = block_norm_pass(a, red);
+  const SumSq bsum = block_norm_pass(a, red);
   norm_arrive(a, bsum, red, &s_flag);
 }
 
-// One block of the final reduction alone: used when there are no chunks and
-// by the no-allocation entry point.
-__global__ void __launch_bounds__(kThreads) k_grad_norm_final(const float2* __restrict__ partials,
-                                                              int64_t n_chunks, float max_norm,
-                                                              float inv_scale, clip_result_t* res,
+// One block of the final reduction alone: the second of the three launches
+// of GCLIP_VARIANT_THREE_KERNEL and of the no-allocation entry point, and
+// the whole clip of an empty set.
+__global__ void __launch_bounds__(kThreads) k_grad_norm_final(const float4* __restrict__ partials,
+                                                              int64_t n, float max_norm,
+                                                              float inv_scale, int tiny_exp,
+                                                              clip_result_t* res,
                                                               float* out_norm, int32_t* out_flag) {
-  __shared__ FF red[kWarps];
+  __shared__ SumSq red[kWarps];
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  final_reduce(partials, n_chunks, max_norm, inv_scale, res, out_norm, out_flag, red);
+  final_reduce(partials, n, max_norm, inv_scale, tiny_exp, res, out_norm, out_flag, red);
 }
 
-__global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __restrict__ chunks,
-                                                         int64_t n_chunks,
+// The clipping page's first kernel ("ANDREA's three-kernel pipeline"): one
+// block per chunk writes that chunk's sum of squares to partials[c].  Used
+// by GCLIP_VARIANT_THREE_KERNEL, per-tensor clipping and the no-allocation
+// entry point.  `clear` (may be NULL): two words zeroed by block 0 before
+// anything else (per-tensor clipping's write list).
+template <class Src>
+__global__ void __launch_bounds__(kThreads) k_chunk_sums(const Src src, float s, float st,
+                                                         float4* __restrict__ partials,
+                                                         unsigned int* clear, int resident) {
+  __shared__ SumSq red[kWarps];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const clip_chunk_t c = src[blockIdx.x];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) clear[0] = clear[1] = 0u;
+  const SumSq acc =
+      chunk_sumsq<HintMem>(c, s, st, red, resident ? policy_evict_normal() : policy_evict_first());
+  if (threadIdx.x == 0) partials[blockIdx.x] = pack(acc);
+}
+
+// The scaling pass, one block per chunk.  The chunk's entry is read only
+// once the block knows it will write (measured: reading it before the wait
+// slowed a clip that writes nothing by 2.4 us on the 120M set, 11,307
+// blocks).
+template <class Src>
+__global__ void __launch_bounds__(kThreads) k_grad_scale(const Src src, int64_t n_chunks,
                                                          const clip_result_t* res) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int decision = res->decision;
@@ -48,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale(const clip_chunk_t* __r
   // (blocks that write nothing trigger by exiting).
   asm volatile("griddepcontrol.launch_dependents;");
   // Highest chunks first: the norm pass read them last and kept them in L2.
-  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const clip_chunk_t c = src[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
   chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
 }
 
@@ -113,21 +140,6 @@ __device__ __forceinline__ void adamw4(const float* x, float4& W, float4& M, flo
   adamw1(x[1], W.y, M.y, V.y, chi, clo, p);
   adamw1(x[2], W.z, M.z, V.z, chi, clo, p);
   adamw1(x[3], W.w, M.w, V.w, chi, clo, p);
-}
-
-template <int DT>
-__device__ __forceinline__ void widen_vec(uint4 g, float (&x)[8]) {
-  if constexpr (DT == GCLIP_F32) {
-    x[0] = __uint_as_float(g.x);
-    x[1] = __uint_as_float(g.y);
-    x[2] = __uint_as_float(g.z);
-    x[3] = __uint_as_float(g.w);
-  } else {
-    const float2 a = Fmt<DT>::widen(g.x), b = Fmt<DT>::widen(g.y), c = Fmt<DT>::widen(g.z),
-                 d = Fmt<DT>::widen(g.w);
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-    x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
-  }
 }
 
 template <int DT>
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) k_to_f32(const clip_chunk_t* __restr
 
 __global__ void __launch_bounds__(kThreads, 5) k_grad_norm_accumulate(const NormArgs a,
                                                                      const TensorState* __restrict__ adds) {
-  __shared__ FF red[kWarps];
+  __shared__ SumSq red[kWarps];
   __shared__ int s_flag;
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -305,57 +317,46 @@ __global__ void __launch_bounds__(kThreads, 5) k_grad_norm_accumulate(const Norm
   // fp32 -4.5 us, fp16 -4.3 us; nothing lost when no scaling pass writes).
   const uint64_t pol_first = a.prefetch ? policy_evict_normal() : policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
-  FF acc = {0.f, 0.f};
+  SumSq acc = {{0.f, 0.f}, {0.f, 0.f}};
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const clip_chunk_t ch = a.chunks[c];
     const TensorState ts = adds[ch.meta >> 8];
-    acc = chunk_add_accumulate(acc, ch, ts.w + (ch.addr - ts.g), a.inv_scale,
-                               c >= a.keep_from ? pol_last : pol_first);
+    chunk_add_accumulate(acc, ch, ts.w + (ch.addr - ts.g), a.inv_scale, a.inv_scale_tiny,
+                         c >= a.keep_from ? pol_last : pol_first);
   }
   norm_arrive(a, block_reduce(acc, red), red, &s_flag);
 }
 
 // ---------------------------------------------------------------------------
 // Per-tensor clipping: each tensor clipped by its own norm.  One block per
-// chunk writes the chunk's sum of squares; one block per tensor reduces its
+// chunk writes the chunk's sum of squares (k_chunk_sums, which also empties
+// the write list); one block per tensor reduces its
 // chunks' sums (the same fixed order as the final reduction), decides, and
 // lists its chunks if they are to be rewritten; a wave of blocks scales the
 // listed chunks, each with its tensor's multiplier.
-
-__global__ void __launch_bounds__(kThreads) k_chunk_partials(const clip_chunk_t* __restrict__ chunks,
-                                                             float inv_scale,
-                                                             float2* __restrict__ partials,
-                                                             unsigned int* wcount) {
-  __shared__ FF red[kWarps];
-  asm volatile("griddepcontrol.launch_dependents;");
-  // Launched after the previous call's scaling kernel has finished (no
-  // programmatic dependence), so the write list can be emptied here.
-  if (blockIdx.x == 0 && threadIdx.x == 0) wcount[0] = wcount[1] = 0u;
-  const FF acc = chunk_sumsq<HintMem>(chunks[blockIdx.x], inv_scale, red, policy_evict_first());
-  if (threadIdx.x == 0) partials[blockIdx.x] = make_float2(acc.hi, acc.lo);
-}
 
 // One block per tensor: the tensor's norm and decision, and, when its
 // elements are to be rewritten, its chunks appended to the write list (in
 // whatever order the tensors finish: each chunk is scaled on its own, so the
 // order changes nothing in the results).
-__global__ void __launch_bounds__(kThreads) k_tensor_final(const float2* __restrict__ partials,
+__global__ void __launch_bounds__(kThreads) k_tensor_final(const float4* __restrict__ partials,
                                                            const int64_t* __restrict__ first,
                                                            float max_norm, float inv_scale,
+                                                           int tiny_exp,
                                                            clip_result_t* recs, float* out_norms,
                                                            int32_t* out_flags,
                                                            int64_t* __restrict__ wlist,
                                                            unsigned int* wcount) {
-  __shared__ FF red[kWarps];
+  __shared__ SumSq red[kWarps];
   __shared__ int64_t s_base;
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int64_t c0 = first[t], nc = first[t + 1] - c0;
   const unsigned int calls = threadIdx.x == 0 ? __ldcg(&recs[t].calls) : 0u;
-  const FF acc = reduce_partials(partials + c0, nc, red);
+  const SumSq acc = reduce_partials(partials + c0, nc, red);
   if (threadIdx.x == 0) {
-    decide_write(acc, max_norm, inv_scale, recs + t, out_norms ? out_norms + t : nullptr,
+    decide_write(acc, max_norm, inv_scale, tiny_exp, recs + t, out_norms ? out_norms + t : nullptr,
                  out_flags ? out_flags + t : nullptr, calls);
     const clip_result_t& r = recs[t];
     s_base = must_write(r.decision, r.coef_hi, r.coef_lo) && nc > 0
@@ -411,9 +412,9 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-__global__ void __launch_bounds__(kThreads, 5) k_clip_persistent(const NormArgs a, SyncWords* sync,
+__global__ void __launch_bounds__(kThreads, 4) k_clip_persistent(const NormArgs a, SyncWords* sync,
                                                               long long timeout_ns) {
-  __shared__ FF red[kWarps];
+  __shared__ SumSq red[kWarps];
   __shared__ unsigned int s_gen0, s_claim;
   __shared__ int s_flag, s_go;
 
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_clip_persistent(const NormArgs 
   if (threadIdx.x == 0) s_gen0 = *reinterpret_cast<volatile unsigned int*>(&sync->gen);
 
   // Phase 1: the norm pass; the block that arrives last publishes the record.
-  const FF bsum = block_norm_pass(a, red);
+  const SumSq bsum = block_norm_pass(a, red);
   const bool published = norm_arrive(a, bsum, red, &s_flag);
 
   if (published) {

@@ -12,61 +12,94 @@
 namespace gclip {
 
 // ---------------------------------------------------------------------------
+// Squares of one vector or one element into the two bins (see SumSq).  The
+// vector's sum r of the squares of y = x * s (the first square, then fused
+// multiply-adds in element order) goes to `big` unless r < kTinySq; such a
+// vector is summed again as the squares of x * st (st = s * 2^K) into
+// `tiny`.  r < 2^-100 means every |y| < 2^-50, and r >= 2^-100 means the
+// squares that underflowed (each off by at most 2^-150) change r by less
+// than 2^-46 of itself.  A NaN or infinite r goes to `big`.  The common case
+// costs one comparison and a branch that is not taken.
+
+template <int DT>
+__device__ __forceinline__ void vec_sumsq(FF& big, FF& tiny, uint4 v, float s, float st) {
+  const float r = Fmt<DT>::sumsq(v, s);
+  if (__builtin_expect(r < kTinySq, 0)) tiny = ff_add_f(tiny, Fmt<DT>::sumsq(v, st));
+  else big = ff_add_f(big, r);
+}
+
+template <int DT>
+__device__ __forceinline__ void vec_sumsq(SumSq& acc, uint4 v, float s, float st) {
+  vec_sumsq<DT>(acc.big, acc.tiny, v, s, st);
+}
+
+__device__ __forceinline__ void elem_sumsq(FF& big, FF& tiny, float x, float s, float st) {
+  const float y = __fmul_rn(x, s);
+  const float r = __fmul_rn(y, y);
+  if (__builtin_expect(r < kTinySq, 0)) {
+    const float z = __fmul_rn(x, st);
+    tiny = ff_add_f(tiny, __fmul_rn(z, z));
+  } else {
+    big = ff_add_f(big, r);
+  }
+}
+
+__device__ __forceinline__ void elem_sumsq(SumSq& acc, float x, float s, float st) {
+  elem_sumsq(acc.big, acc.tiny, x, s, st);
+}
+
+// ---------------------------------------------------------------------------
 // Sum of squares of one chunk: this thread's share, in a fixed order.
 
 template <int DT, class M>
-__device__ __forceinline__ FF chunk_sumsq_thread(FF acc, uint64_t addr, uint32_t n, float s,
-                                                 uint64_t pol) {
+__device__ __forceinline__ void chunk_sumsq_thread(SumSq& acc, uint64_t addr, uint32_t n, float s,
+                                                   float st, uint64_t pol) {
   const Span sp = make_span<DT>(addr, n);
   const uint4* v = reinterpret_cast<const uint4*>(sp.body);
-  for (uint32_t base = threadIdx.x; base < sp.nvec; base += kUnroll * kThreads) {
-    uint4 buf[kUnroll];
+  for (uint32_t base = threadIdx.x; base < sp.nvec; base += kNormUnroll * kThreads) {
+    uint4 buf[kNormUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kNormUnroll; ++u) {
       const uint32_t i = base + u * kThreads;
       buf[u] = i < sp.nvec ? M::ld_norm(v + i, pol) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (base + u * kThreads < sp.nvec) acc = ff_add_f(acc, Fmt<DT>::sumsq(buf[u], s));
+    for (int u = 0; u < kNormUnroll; ++u) {
+      if (base + u * kThreads < sp.nvec) vec_sumsq<DT>(acc, buf[u], s, st);
     }
   }
   constexpr uint32_t B = Fmt<DT>::kBytes;
-  if (threadIdx.x < sp.head) {
-    const float y = __fmul_rn(Fmt<DT>::load1(addr + threadIdx.x * B), s);
-    acc = ff_add_f(acc, __fmul_rn(y, y));
-  }
-  if (threadIdx.x < sp.ntail) {
-    const float y =
-        __fmul_rn(Fmt<DT>::load1(addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B), s);
-    acc = ff_add_f(acc, __fmul_rn(y, y));
-  }
-  return acc;
+  if (threadIdx.x < sp.head) elem_sumsq(acc, Fmt<DT>::load1(addr + threadIdx.x * B), s, st);
+  if (threadIdx.x < sp.ntail)
+    elem_sumsq(acc, Fmt<DT>::load1(addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B), s,
+               st);
 }
 
 // Fixed-shape tree over the block; the total is valid in thread 0.  `red`
 // holds kWarps entries; the trailing barrier lets the caller reuse it.
-__device__ __forceinline__ FF block_reduce(FF v, FF* red) {
+__device__ __forceinline__ FF warp_reduce(FF v, int width) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
+    if (off >= width) continue;
     FF o;
     o.hi = __shfl_down_sync(0xffffffffu, v.hi, off);
     o.lo = __shfl_down_sync(0xffffffffu, v.lo, off);
     v = ff_add(v, o);
   }
+  return v;
+}
+
+__device__ __forceinline__ SumSq block_reduce(SumSq v, SumSq* red) {
+  v.big = warp_reduce(v.big, 32);
+  v.tiny = warp_reduce(v.tiny, 32);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  FF r = {0.f, 0.f};
+  SumSq r = {{0.f, 0.f}, {0.f, 0.f}};
   if (warp == 0) {
-    r = lane < kWarps ? red[lane] : FF{0.f, 0.f};
-#pragma unroll
-    for (int off = kWarps / 2; off > 0; off >>= 1) {
-      FF o;
-      o.hi = __shfl_down_sync(0xffffffffu, r.hi, off);
-      o.lo = __shfl_down_sync(0xffffffffu, r.lo, off);
-      r = ff_add(r, o);
-    }
+    if (lane < kWarps) r = red[lane];
+    r.big = warp_reduce(r.big, kWarps);
+    r.tiny = warp_reduce(r.tiny, kWarps);
   }
   __syncthreads();
   return r;
@@ -74,18 +107,26 @@ __device__ __forceinline__ FF block_reduce(FF v, FF* red) {
 
 // Add this thread's share of chunk `c` to its running accumulator.
 template <class M>
-__device__ __forceinline__ FF chunk_accumulate(FF acc, const clip_chunk_t& c, float s, uint64_t pol) {
+__device__ __forceinline__ void chunk_accumulate(SumSq& acc, const clip_chunk_t& c, float s, float st,
+                                                 uint64_t pol) {
   switch (c.meta & 0xffu) {
-    case GCLIP_F32: return chunk_sumsq_thread<GCLIP_F32, M>(acc, c.addr, c.numel, s, pol);
-    case GCLIP_F16: return chunk_sumsq_thread<GCLIP_F16, M>(acc, c.addr, c.numel, s, pol);
-    default: return chunk_sumsq_thread<GCLIP_BF16, M>(acc, c.addr, c.numel, s, pol);
+    case GCLIP_F32: chunk_sumsq_thread<GCLIP_F32, M>(acc, c.addr, c.numel, s, st, pol); break;
+    case GCLIP_F16: chunk_sumsq_thread<GCLIP_F16, M>(acc, c.addr, c.numel, s, st, pol); break;
+    default: chunk_sumsq_thread<GCLIP_BF16, M>(acc, c.addr, c.numel, s, st, pol); break;
   }
 }
 
 // The sum of squares of one chunk, valid in thread 0.
 template <class M>
-__device__ __forceinline__ FF chunk_sumsq(const clip_chunk_t& c, float s, FF* red, uint64_t pol) {
-  return block_reduce(chunk_accumulate<M>(FF{0.f, 0.f}, c, s, pol), red);
+__device__ __forceinline__ SumSq chunk_sumsq(const clip_chunk_t& c, float s, float st, SumSq* red,
+                                             uint64_t pol) {
+  SumSq acc = {{0.f, 0.f}, {0.f, 0.f}};
+  chunk_accumulate<M>(acc, c, s, st, pol);
+  return block_reduce(acc, red);
+}
+
+__device__ __forceinline__ float4 pack(SumSq a) {
+  return make_float4(a.big.hi, a.big.lo, a.tiny.hi, a.tiny.lo);
 }
 
 // ---------------------------------------------------------------------------
@@ -119,16 +160,16 @@ __device__ __forceinline__ uint4 load_vec_elems(uint64_t a) {
 
 // One scalar element: x + a rounded to the format, stored, squared.
 template <int DT>
-__device__ __forceinline__ FF add_sumsq1(FF acc, uint64_t x_at, uint64_t a_at, float s) {
+__device__ __forceinline__ void add_sumsq1(SumSq& acc, uint64_t x_at, uint64_t a_at, float s,
+                                           float st) {
   const float r = Fmt<DT>::round1(__fadd_rn(Fmt<DT>::load1(x_at), Fmt<DT>::load1(a_at)));
   Fmt<DT>::store1(x_at, r);
-  const float y = __fmul_rn(r, s);
-  return ff_add_f(acc, __fmul_rn(y, y));
+  elem_sumsq(acc, r, s, st);
 }
 
 template <int DT>
-__device__ __forceinline__ FF chunk_add_sumsq_thread(FF acc, uint64_t addr, uint64_t add_addr,
-                                                     uint32_t n, float s, uint64_t pol) {
+__device__ __forceinline__ void chunk_add_sumsq_thread(SumSq& acc, uint64_t addr, uint64_t add_addr,
+                                                       uint32_t n, float s, float st, uint64_t pol) {
   constexpr uint32_t B = Fmt<DT>::kBytes;
   const Span sp = make_span<DT>(addr, n);
   uint4* v = reinterpret_cast<uint4*>(sp.body);
@@ -155,25 +196,25 @@ __device__ __forceinline__ FF chunk_add_sumsq_thread(FF acc, uint64_t addr, uint
       if (i < sp.nvec) {
         const uint4 sum = Fmt<DT>::add(x[u], a[u]);
         HintMem::st_scale(v + i, sum, pol);
-        acc = ff_add_f(acc, Fmt<DT>::sumsq(sum, s));
+        vec_sumsq<DT>(acc, sum, s, st);
       }
     }
   }
   if (threadIdx.x < sp.head)
-    acc = add_sumsq1<DT>(acc, addr + threadIdx.x * B, add_addr + threadIdx.x * B, s);
+    add_sumsq1<DT>(acc, addr + threadIdx.x * B, add_addr + threadIdx.x * B, s, st);
   if (threadIdx.x < sp.ntail) {
     const uint64_t off = static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B;
-    acc = add_sumsq1<DT>(acc, addr + off, add_addr + off, s);
+    add_sumsq1<DT>(acc, addr + off, add_addr + off, s, st);
   }
-  return acc;
 }
 
-__device__ __forceinline__ FF chunk_add_accumulate(FF acc, const clip_chunk_t& c, uint64_t add_addr,
-                                                   float s, uint64_t pol) {
+__device__ __forceinline__ void chunk_add_accumulate(SumSq& acc, const clip_chunk_t& c,
+                                                     uint64_t add_addr, float s, float st,
+                                                     uint64_t pol) {
   switch (c.meta & 0xffu) {
-    case GCLIP_F32: return chunk_add_sumsq_thread<GCLIP_F32>(acc, c.addr, add_addr, c.numel, s, pol);
-    case GCLIP_F16: return chunk_add_sumsq_thread<GCLIP_F16>(acc, c.addr, add_addr, c.numel, s, pol);
-    default: return chunk_add_sumsq_thread<GCLIP_BF16>(acc, c.addr, add_addr, c.numel, s, pol);
+    case GCLIP_F32: chunk_add_sumsq_thread<GCLIP_F32>(acc, c.addr, add_addr, c.numel, s, st, pol); break;
+    case GCLIP_F16: chunk_add_sumsq_thread<GCLIP_F16>(acc, c.addr, add_addr, c.numel, s, st, pol); break;
+    default: chunk_add_sumsq_thread<GCLIP_BF16>(acc, c.addr, add_addr, c.numel, s, st, pol); break;
   }
 }
 
@@ -226,36 +267,44 @@ __device__ __forceinline__ bool must_write(int decision, float chi, float clo) {
 // Final reduction over partial sums, square root and decision.  Runs on one
 // block of kThreads threads: thread t sums entries t, t + kThreads, ... in
 // increasing order, then the fixed block tree; thread 0 writes the record.
+// An entry is one SumSq packed as float4 {big.hi, big.lo, tiny.hi, tiny.lo}.
 //
-// The decision is taken in double from the float-float sum: S = hi + lo is
-// exact in double, norm = sqrt(S) and max_norm / norm are IEEE double
-// operations, and the multiplier inv_scale * max_norm / norm is handed to the
-// scaling pass as a float-float pair so that each output is rounded once.
+// The decision is taken in double: S = big + tiny * 2^-2K is formed in double
+// (each float-float bin exactly, one rounding for the sum), norm = sqrt(S)
+// and max_norm / norm are IEEE double operations, and the multiplier
+// inv_scale * max_norm / norm is handed to the scaling pass as a float-float
+// pair so that each output is rounded once.
 
-__device__ FF reduce_partials(const float2* partials, int64_t n, FF* red) {
-  FF acc = {0.f, 0.f};
+__device__ SumSq reduce_partials(const float4* partials, int64_t n, SumSq* red) {
+  SumSq acc = {{0.f, 0.f}, {0.f, 0.f}};
   // Up to four entries loaded at once, then added in increasing index order:
   // thread t's sum is always entries t, t + kThreads, t + 2 kThreads, ...
   for (int64_t c = threadIdx.x; c < n; c += 4 * kThreads) {
-    float2 p[4];
+    float4 p[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i = c + u * kThreads;
-      p[u] = i < n ? __ldcg(partials + i) : make_float2(0.f, 0.f);
+      p[u] = i < n ? __ldcg(partials + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (c + u * kThreads < n) acc = ff_add(acc, FF{p[u].x, p[u].y});
+      if (c + u * kThreads < n) acc = sumsq_add(acc, SumSq{{p[u].x, p[u].y}, {p[u].z, p[u].w}});
   }
   return block_reduce(acc, red);
 }
 
-// The norm, flag, decision and multiplier from the float-float sum of
-// squares S = hi + lo (thread 0).
-__device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_result_t* res,
-                             float* out_norm, int32_t* out_flag, unsigned int calls) {
-  const double S = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
-  const bool nonfinite = !isfinite(acc.hi) || !isfinite(acc.lo) || S > static_cast<double>(FLT_MAX);
+// The norm, flag, decision and multiplier from the two-bin sum of squares
+// (thread 0).  `tiny_exp` is the K of the call (the tiny bin holds squares
+// scaled by 2^2K).
+__device__ void decide_write(SumSq acc, float max_norm, float inv_scale, int tiny_exp,
+                             clip_result_t* res, float* out_norm, int32_t* out_flag,
+                             unsigned int calls) {
+  const double big = static_cast<double>(acc.big.hi) + static_cast<double>(acc.big.lo);
+  const double tiny = static_cast<double>(acc.tiny.hi) + static_cast<double>(acc.tiny.lo);
+  const double S = big + ldexp(tiny, -2 * tiny_exp);
+  const bool nonfinite = !isfinite(acc.big.hi) || !isfinite(acc.big.lo) ||
+                         !isfinite(acc.tiny.hi) || !isfinite(acc.tiny.lo) ||
+                         S > static_cast<double>(FLT_MAX);
   const double norm = sqrt(S);
   int decision;
   float chi = 1.0f, clo = 0.0f;
@@ -271,27 +320,59 @@ __device__ void decide_write(FF acc, float max_norm, float inv_scale, clip_resul
     chi = inv_scale;
   }
   const float norm_f = __double2float_rn(norm);
+  const float s_hi = __double2float_rn(S);
   res->norm = norm_f;
   res->nonfinite = nonfinite ? 1 : 0;
   res->decision = decision;
   res->coef_hi = chi;
   res->coef_lo = clo;
-  res->sumsq_hi = acc.hi;
-  res->sumsq_lo = acc.lo;
+  res->sumsq_hi = s_hi;
+  res->sumsq_lo = __double2float_rn(S - static_cast<double>(s_hi));
   res->calls = calls + 1u;  // `calls`: the count read before the reduction
   if (out_norm) *out_norm = norm_f;
   if (out_flag) *out_flag = nonfinite ? 1 : 0;
 }
 
-__device__ void final_reduce(const float2* partials, int64_t n_chunks, float max_norm,
-                             float inv_scale, clip_result_t* res, float* out_norm,
-                             int32_t* out_flag, FF* red) {
+__device__ void final_reduce(const float4* partials, int64_t n, float max_norm, float inv_scale,
+                             int tiny_exp, clip_result_t* res, float* out_norm, int32_t* out_flag,
+                             SumSq* red) {
   // The record's call count, loaded now so that its latency overlaps the
   // reduction instead of following it.
   const unsigned int calls = threadIdx.x == 0 ? __ldcg(&res->calls) : 0u;
-  const FF acc = reduce_partials(partials, n_chunks, red);
-  if (threadIdx.x == 0) decide_write(acc, max_norm, inv_scale, res, out_norm, out_flag, calls);
+  const SumSq acc = reduce_partials(partials, n, red);
+  if (threadIdx.x == 0)
+    decide_write(acc, max_norm, inv_scale, tiny_exp, res, out_norm, out_flag, calls);
 }
+
+// ---------------------------------------------------------------------------
+// Where a kernel finds chunk c: the handle's chunk table, or one contiguous
+// buffer cut on the fly exactly as the host planner cuts a single tensor
+// (the first chunk takes the elements before the first 16-byte boundary
+// plus a full chunk, every later chunk starts aligned).
+
+struct TableChunks {
+  const clip_chunk_t* chunks;
+  __device__ __forceinline__ clip_chunk_t operator[](int64_t c) const { return chunks[c]; }
+};
+
+struct FlatChunks {
+  uint64_t base;
+  int64_t numel;
+  int32_t dtype;
+  __device__ __forceinline__ clip_chunk_t operator[](int64_t c) const {
+    const int64_t es = dtype == GCLIP_F32 ? 4 : 2;
+    const int64_t per = GCLIP_CHUNK_BYTES / es;
+    const int64_t head = static_cast<int64_t>((16u - (base & 15u)) & 15u) / es;
+    const int64_t start = c == 0 ? 0 : head + c * per;
+    const int64_t want = c == 0 ? head + per : per;
+    const int64_t left = numel - start;
+    clip_chunk_t ch;
+    ch.addr = base + static_cast<uint64_t>(start * es);
+    ch.numel = static_cast<uint32_t>(left < want ? left : want);
+    ch.meta = static_cast<uint32_t>(dtype);
+    return ch;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // The norm pass of the handle-based clip, shared by the register-engine
@@ -305,24 +386,25 @@ __device__ void final_reduce(const float2* partials, int64_t n_chunks, float max
 // pass, which visits them first, starts.  On a 4.9 GB set the extra requests
 // cost 1%, so larger sets are not prefetched.  The arithmetic is unchanged.
 //
-// A grid of G blocks (G fixed per handle: the co-resident count of the
-// single-launch kernel, at most the number of chunks).  Block b takes chunks
-// b, b + G, b + 2G, ...; each of its threads keeps one float-float
-// accumulator over its share of all those chunks, in that order, and the
-// block tree combines the threads once at the end.  The block sum goes to
-// block_sums[b]; the block that arrives last reduces the G block sums in
-// fixed order (final_reduce) and publishes the record.  Which block arrives
-// last depends on timing; the arithmetic does not.
+// A grid of G blocks (G fixed per handle).  Block b takes chunks b, b + G,
+// b + 2G, ...; each of its threads keeps one two-bin accumulator over its
+// share of all those chunks, in that order, and the block tree combines the
+// threads once at the end.  The block sum goes to block_sums[b]; the block
+// that arrives last reduces the G block sums in fixed order (final_reduce)
+// and publishes the record.  Which block arrives last depends on timing; the
+// arithmetic does not.
 
 struct NormArgs {
   const clip_chunk_t* chunks;
   int64_t n_chunks;
-  float2* block_sums;     // G entries
+  float4* block_sums;     // G entries
   unsigned int* arrive;   // blocks done with the norm pass in this call
   unsigned int* work;     // chunks the scaling pass claims in this call
   unsigned int expected;  // G, plus the test hook's extra arrivals
   float max_norm;
   float inv_scale;
+  float inv_scale_tiny;   // inv_scale * 2^tiny_exp, exact
+  int tiny_exp;
   clip_result_t* res;
   float* out_norm;
   int32_t* out_flag;
@@ -331,34 +413,39 @@ struct NormArgs {
   int prefetch;           // each block asks L2 for its next chunk ahead of its loads
 };
 
-__device__ __forceinline__ FF block_norm_pass(const NormArgs& a, FF* red) {
+// This block's chunk c: its share into `acc`, after a bulk L2 prefetch of
+// the aligned body of its next chunk (when the set is prefetched).
+__device__ __forceinline__ void norm_chunk(const NormArgs& a, int64_t c, const clip_chunk_t& ch,
+                                           SumSq& acc, uint64_t pol_first, uint64_t pol_last) {
+  if (a.prefetch && threadIdx.x == 0 && c + gridDim.x < a.n_chunks) {
+    const clip_chunk_t nx = a.chunks[c + gridDim.x];
+    const uint32_t es = (nx.meta & 0xffu) == GCLIP_F32 ? 4u : 2u;
+    const uint32_t head = min(nx.numel, static_cast<uint32_t>(((16u - (nx.addr & 15u)) & 15u) / es));
+    const uint32_t bytes = (nx.numel - head) / (16u / es) * 16u;
+    if (bytes)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nx.addr + head * es), "r"(bytes)
+                   : "memory");
+  }
+  chunk_accumulate<HintMem>(acc, ch, a.inv_scale, a.inv_scale_tiny,
+                            c >= a.keep_from ? pol_last : pol_first);
+}
+
+__device__ __forceinline__ SumSq block_norm_pass(const NormArgs& a, SumSq* red) {
   // A set that fits in L2 may stay there for the next call; a larger one is
   // streamed through without displacing anything.
   const uint64_t pol_first = a.resident ? policy_evict_normal() : policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
-  FF acc = {0.f, 0.f};
-  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
-    const clip_chunk_t ch = a.chunks[c];
-    if (a.prefetch && threadIdx.x == 0 && c + gridDim.x < a.n_chunks) {
-      // One bulk request for the aligned body of this block's next chunk.
-      const clip_chunk_t nx = a.chunks[c + gridDim.x];
-      const uint32_t es = (nx.meta & 0xffu) == GCLIP_F32 ? 4u : 2u;
-      const uint32_t head = min(nx.numel, static_cast<uint32_t>(((16u - (nx.addr & 15u)) & 15u) / es));
-      const uint32_t bytes = (nx.numel - head) / (16u / es) * 16u;
-      if (bytes)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nx.addr + head * es), "r"(bytes)
-                     : "memory");
-    }
-    acc = chunk_accumulate<HintMem>(acc, ch, a.inv_scale, c >= a.keep_from ? pol_last : pol_first);
-  }
+  SumSq acc = {{0.f, 0.f}, {0.f, 0.f}};
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x)
+    norm_chunk(a, c, a.chunks[c], acc, pol_first, pol_last);
   return block_reduce(acc, red);
 }
 
 // Publish this block's sum; returns true (in every thread) in the block that
 // arrived last, after it has written the record.
-__device__ __forceinline__ bool norm_arrive(const NormArgs& a, FF bsum, FF* red, int* s_flag) {
+__device__ __forceinline__ bool norm_arrive(const NormArgs& a, SumSq bsum, SumSq* red, int* s_flag) {
   if (threadIdx.x == 0) {
-    a.block_sums[blockIdx.x] = make_float2(bsum.hi, bsum.lo);
+    a.block_sums[blockIdx.x] = pack(bsum);
     // One acquire-release ticket: the release publishes this block's sum
     // with the increment; the acquire in the block that takes the last
     // ticket makes every earlier block's sum visible to it (the increments
@@ -370,8 +457,8 @@ __device__ __forceinline__ bool norm_arrive(const NormArgs& a, FF bsum, FF* red,
   }
   __syncthreads();
   if (!*s_flag) return false;
-  final_reduce(a.block_sums, gridDim.x, a.max_norm, a.inv_scale, a.res, a.out_norm, a.out_flag,
-               red);
+  final_reduce(a.block_sums, gridDim.x, a.max_norm, a.inv_scale, a.tiny_exp, a.res, a.out_norm,
+               a.out_flag, red);
   if (threadIdx.x == 0) {
     // No fence: the end of the kernel orders these stores and the record
     // before the dependent launch; the single-launch kernels fence before

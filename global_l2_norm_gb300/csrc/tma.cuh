@@ -179,36 +179,32 @@ __device__ __forceinline__ bool ring_aborted(const Ring& r, int64_t k, int64_t i
 }
 
 // This thread's share of one staged chunk, added to four independent
-// accumulators (vector j of the thread's share goes to acc[j % 4]) so that
+// accumulators (vector j of the thread's share goes to big[j % 4]) so that
 // four float-float chains run side by side; head and tail scalars go to
-// acc[0].  The order is fixed, so the result is deterministic.
+// big[0].  Vectors and scalars of tiny elements go to the one `tiny` bin
+// (see SumSq).  The order is fixed, so the result is deterministic.
 template <int DT>
-__device__ __forceinline__ void stage_sumsq(FF (&acc)[4], const uint8_t* st, const clip_chunk_t& c,
-                                            float s) {
+__device__ __forceinline__ void stage_sumsq(FF (&big)[4], FF& tiny, const uint8_t* st,
+                                            const clip_chunk_t& c, float s, float sti) {
   const Span sp = make_span<DT>(c.addr, c.numel);
   const uint4* v = reinterpret_cast<const uint4*>(st);
   uint32_t i = threadIdx.x;
   for (; i + 3 * kThreads < sp.nvec; i += 4 * kThreads) {
     const uint4 v0 = v[i], v1 = v[i + kThreads], v2 = v[i + 2 * kThreads], v3 = v[i + 3 * kThreads];
-    acc[0] = ff_add_f(acc[0], Fmt<DT>::sumsq(v0, s));
-    acc[1] = ff_add_f(acc[1], Fmt<DT>::sumsq(v1, s));
-    acc[2] = ff_add_f(acc[2], Fmt<DT>::sumsq(v2, s));
-    acc[3] = ff_add_f(acc[3], Fmt<DT>::sumsq(v3, s));
+    vec_sumsq<DT>(big[0], tiny, v0, s, sti);
+    vec_sumsq<DT>(big[1], tiny, v1, s, sti);
+    vec_sumsq<DT>(big[2], tiny, v2, s, sti);
+    vec_sumsq<DT>(big[3], tiny, v3, s, sti);
   }
-  // fewer than four vectors left: constant indices keep acc in registers
-  if (i < sp.nvec) acc[0] = ff_add_f(acc[0], Fmt<DT>::sumsq(v[i], s));
-  if (i + kThreads < sp.nvec) acc[1] = ff_add_f(acc[1], Fmt<DT>::sumsq(v[i + kThreads], s));
-  if (i + 2 * kThreads < sp.nvec) acc[2] = ff_add_f(acc[2], Fmt<DT>::sumsq(v[i + 2 * kThreads], s));
+  // fewer than four vectors left: constant indices keep the bins in registers
+  if (i < sp.nvec) vec_sumsq<DT>(big[0], tiny, v[i], s, sti);
+  if (i + kThreads < sp.nvec) vec_sumsq<DT>(big[1], tiny, v[i + kThreads], s, sti);
+  if (i + 2 * kThreads < sp.nvec) vec_sumsq<DT>(big[2], tiny, v[i + 2 * kThreads], s, sti);
   constexpr uint32_t B = Fmt<DT>::kBytes;
-  if (threadIdx.x < sp.head) {
-    const float y = __fmul_rn(Fmt<DT>::load1(c.addr + threadIdx.x * B), s);
-    acc[0] = ff_add_f(acc[0], __fmul_rn(y, y));
-  }
-  if (threadIdx.x < sp.ntail) {
-    const float y =
-        __fmul_rn(Fmt<DT>::load1(c.addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B), s);
-    acc[0] = ff_add_f(acc[0], __fmul_rn(y, y));
-  }
+  if (threadIdx.x < sp.head) elem_sumsq(big[0], tiny, Fmt<DT>::load1(c.addr + threadIdx.x * B), s, sti);
+  if (threadIdx.x < sp.ntail)
+    elem_sumsq(big[0], tiny,
+               Fmt<DT>::load1(c.addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B), s, sti);
 }
 
 template <int DT>
@@ -239,8 +235,8 @@ __device__ __forceinline__ int64_t my_count(int64_t n) {
 
 // Norm pass through the ring; the block sum is valid in thread 0.  Returns
 // false (uniformly) if a copy timed out; no copy is then in flight.
-__device__ bool tma_norm_pass(const NormArgs& a, const Ring& r, uint32_t& phase, FF* red,
-                              volatile int* s_abort, FF* out) {
+__device__ bool tma_norm_pass(const NormArgs& a, const Ring& r, uint32_t& phase, SumSq* red,
+                              volatile int* s_abort, SumSq* out) {
   const int64_t mine = my_count(a.n_chunks);
   const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
   int64_t issued = 0;
@@ -252,14 +248,15 @@ __device__ bool tma_norm_pass(const NormArgs& a, const Ring& r, uint32_t& phase,
     }
   }
   FF acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  FF tiny = {0.f, 0.f};
   for (int64_t k = 0; k < mine; ++k) {
     const int s = static_cast<int>(k % kStages);
     if (ring_wait(r, k, phase, a.res, s_abort)) {
       const clip_chunk_t ch = a.chunks[norm_chunk(k)];
       switch (ch.meta & 0xffu) {
-        case GCLIP_F32: stage_sumsq<GCLIP_F32>(acc, r.stage(s), ch, a.inv_scale); break;
-        case GCLIP_F16: stage_sumsq<GCLIP_F16>(acc, r.stage(s), ch, a.inv_scale); break;
-        default: stage_sumsq<GCLIP_BF16>(acc, r.stage(s), ch, a.inv_scale); break;
+        case GCLIP_F32: stage_sumsq<GCLIP_F32>(acc, tiny, r.stage(s), ch, a.inv_scale, a.inv_scale_tiny); break;
+        case GCLIP_F16: stage_sumsq<GCLIP_F16>(acc, tiny, r.stage(s), ch, a.inv_scale, a.inv_scale_tiny); break;
+        default: stage_sumsq<GCLIP_BF16>(acc, tiny, r.stage(s), ch, a.inv_scale, a.inv_scale_tiny); break;
       }
     }
     __syncthreads();
@@ -271,7 +268,7 @@ __device__ bool tma_norm_pass(const NormArgs& a, const Ring& r, uint32_t& phase,
       ++issued;
     }
   }
-  *out = block_reduce(ff_add(ff_add(acc[0], acc[1]), ff_add(acc[2], acc[3])), red);
+  *out = block_reduce(SumSq{ff_add(ff_add(acc[0], acc[1]), ff_add(acc[2], acc[3])), tiny}, red);
   return true;
 }
 
@@ -333,17 +330,17 @@ __device__ bool tma_scale_pass(const clip_chunk_t* chunks, int64_t n, const Ring
 
 __global__ void __launch_bounds__(kThreads, 2) k_norm_tma(const NormArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ FF red[kWarps];
+  __shared__ SumSq red[kWarps];
   __shared__ int s_abort, s_flag;
   asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) s_abort = 0;
   const Ring r = ring_setup(smem);
   uint32_t phase = 0;
-  FF bsum;
+  SumSq bsum;
   // A block whose copy timed out still arrives, with a NaN sum, so that the
   // record is published and says SKIP.
   if (!tma_norm_pass(a, r, phase, red, &s_abort, &bsum) && threadIdx.x == 0)
-    bsum = FF{__int_as_float(0x7fc00000), 0.f};
+    bsum = SumSq{{__int_as_float(0x7fc00000), 0.f}, {0.f, 0.f}};
   norm_arrive(a, bsum, red, &s_flag);
 }
 
@@ -374,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_scale_tma(const clip_chunk_t* _
 __global__ void __launch_bounds__(kThreads, 2) k_clip_persistent_tma(const NormArgs a, SyncWords* sync,
                                                                      long long timeout_ns) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ FF red[kWarps];
+  __shared__ SumSq red[kWarps];
   __shared__ unsigned int s_gen0;
   __shared__ int s_abort, s_flag, s_go;
   if (threadIdx.x == 0) {
@@ -383,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_clip_persistent_tma(const NormA
   }
   const Ring r = ring_setup(smem);
   uint32_t phase = 0;
-  FF bsum;
+  SumSq bsum;
   const bool ok = tma_norm_pass(a, r, phase, red, &s_abort, &bsum);
   // A block whose copy timed out still arrives, with a NaN sum (so the clip
   // is skipped), to keep the others from waiting for it.
-  if (!ok && threadIdx.x == 0) bsum = FF{__int_as_float(0x7fc00000), 0.f};
+  if (!ok && threadIdx.x == 0) bsum = SumSq{{__int_as_float(0x7fc00000), 0.f}, {0.f, 0.f}};
   const bool published = norm_arrive(a, bsum, red, &s_flag);
 
   // Speculative prefetch of the scaling pass while the record is pending.

@@ -78,6 +78,12 @@ extern "C" {
                                        about 0.5% when every element is
                                        written, faster when nothing is
                                        (few blocks to retire)               */
+#define GCLIP_VARIANT_THREE_KERNEL 5  /* the clipping page's pipeline as
+                                       written: one block per chunk writes
+                                       that chunk's sum of squares, one
+                                       block reduces them and decides, one
+                                       block per chunk scales (three
+                                       launches)                            */
 
 /* One gradient tensor: `numel` elements of format `dtype`, contiguous, in
  * device memory at `ptr` (aligned to the element size).  `reserved` must be
@@ -93,7 +99,8 @@ typedef struct {
  * that was applied to every element x is coef_hi + coef_lo (a float-float
  * pair; the product x * inv_scale * max_norm / norm for CLIP, x * inv_scale
  * for PASS).  sumsq_hi + sumsq_lo is the sum of squares of the unscaled
- * gradients. */
+ * gradients (the double-precision total rounded to a float-float pair, so
+ * it underflows for sums below about 1e-38 even where the norm does not). */
 typedef struct {
     float norm;          /* global norm of the unscaled gradients (fp32)   */
     int32_t nonfinite;   /* 1 if an element is NaN/inf or the sum of
@@ -167,10 +174,16 @@ int clip_create(const clip_tensor_desc_t *descs, int32_t n_tensors,
  * that multiplier is exactly 1 nothing is written at all.  Results are rounded
  * to nearest-even into the tensor's own format.
  *
- * The sum is taken in a fixed order (per chunk, then over chunks) with a
- * float-float accumulator, so the norm is bit-identical from run to run and
+ * The sum is taken in a fixed order (per chunk, then over chunks) with
+ * float-float accumulators, so the norm is bit-identical from run to run and
  * between the SPLIT, SPLIT_WAVE and PERSISTENT variants (the two TMA variants
- * share another fixed order).
+ * share another fixed order, THREE_KERNEL a third).  Squares are fp32, in two
+ * bins: elements whose unscaled magnitude is below 2^-60 are summed scaled
+ * by a power of two, so that their squares neither underflow nor lose
+ * precision; the bins are combined in double.  The norm is therefore
+ * accurate to about one fp32 ulp for gradients of any magnitude down to the
+ * smallest fp32 values (below about 1e-40, where the fp32 norm itself is
+ * subnormal, it is accurate to an fp32 ulp of that range).
  *
  * max_norm: threshold c, finite and > 0.  inv_scale: finite and > 0.
  * out_norm: device float, may be NULL; receives the norm (fp32).
@@ -187,8 +200,9 @@ int clip_grad_norm(clip_handle_t h, float max_norm, float inv_scale,
 /* clip_grad_norm_profiled -- clip_grad_norm that also records four CUDA
  * events (cudaEvent_t handles created by the caller on the handle's device)
  * on `stream`: events[0] before the first launch, events[1] and events[2]
- * after the norm pass (partial sums and final reduction, one launch),
- * events[3] after the scaling pass.  With the single-launch variant the one
+ * after the norm pass (partial sums and final reduction, one launch; with
+ * GCLIP_VARIANT_THREE_KERNEL events[1] after the per-chunk sums and
+ * events[2] after the final reduction), events[3] after the scaling pass.  With the single-launch variant the one
  * launch lies between events[2] and events[3], and events[1] and events[2]
  * are recorded with events[0].  Programmatic dependent launch is not used in
  * this mode, so the launches do not overlap their neighbours; it is meant
@@ -207,9 +221,9 @@ int clip_destroy(clip_handle_t h);
 /* clip_set_variant -- choose one of the GCLIP_VARIANT_* values for later
  * calls (GCLIP_VARIANT_SPLIT is the default).  SPLIT, SPLIT_WAVE and
  * PERSISTENT compute bit-identical norms and outputs, and so do SPLIT_TMA and
- * PERSISTENT_TMA;
- * the two pairs sum in a different (fixed) order, so their norms can differ
- * in the last bits.  Returns GCLIP_ERR_INVALID_ARG for an unknown variant,
+ * PERSISTENT_TMA; THREE_KERNEL sums each chunk on its own first.  The three
+ * groups sum in different (fixed) orders, so their norms can differ in the
+ * last bits.  Returns GCLIP_ERR_INVALID_ARG for an unknown variant,
  * GCLIP_ERR_UNSUPPORTED if the device cannot launch cooperative kernels. */
 int clip_set_variant(clip_handle_t h, int32_t variant);
 
@@ -225,6 +239,14 @@ const clip_result_t *clip_result_device(clip_handle_t h);
  * `stream` (inspection and tests; not for the training loop).  Returns
  * GCLIP_ERR_INVALID_ARG for NULL arguments, GCLIP_ERR_CUDA on failure. */
 int clip_read_result(clip_handle_t h, clip_result_t *out, void *stream);
+
+/* clip_last_status -- enqueue on `stream` a copy of the status word of the
+ * handle's record (GCLIP_STATUS_OK, or GCLIP_STATUS_TIMEOUT after a
+ * single-launch call whose grid barrier gave up) into the device int32 at
+ * d_out, in stream order after the calls before it; no host sync, no
+ * allocation.  The same word is clip_result_device(h)->status.  Returns
+ * GCLIP_OK, GCLIP_ERR_INVALID_ARG (NULL handle or d_out) or GCLIP_ERR_CUDA. */
+int clip_last_status(clip_handle_t h, int32_t *d_out, void *stream);
 
 /* clip_reset -- enqueue a clear of the handle's grid-barrier words and of
  * the status in its record.  Needed only after a call reported
@@ -454,9 +476,13 @@ int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float inv_scale,
  * which every GPU that loads the library holds until the process exits.
  *
  * grads: `numel` elements of format `dtype` in device memory of the current
- *   device, contiguous, aligned to the element size; clipped in place exactly
- *   as clip_grad_norm clips a handle made of this one tensor (same chunks,
- *   same arithmetic, bit-identical results).
+ *   device, contiguous, aligned to the element size; clipped in place by the
+ *   three launches of GCLIP_VARIANT_THREE_KERNEL, with the buffer cut into
+ *   the chunks clip_create cuts a single tensor into.  The norm, record and
+ *   outputs are bit-identical to clip_grad_norm on a handle made of this one
+ *   tensor with GCLIP_VARIANT_THREE_KERNEL, and agree with the default
+ *   variant within the parity tolerances (that variant sums the same chunks
+ *   in another fixed order).
  * max_norm, inv_scale, out_norm, out_nonfinite_flag, stream: as for
  *   clip_grad_norm; the stream must belong to the current device.
  * Limit: the buffer may span at most GCLIP_NOALLOC_MAX_CHUNKS chunks of
@@ -465,21 +491,24 @@ int clip_grad_norm_accumulate(clip_handle_t h, float max_norm, float inv_scale,
  *   16-byte boundary); a larger buffer returns GCLIP_ERR_TOO_LARGE and
  *   nothing is enqueued.
  * Set-up: the first call on each device looks up the device address of the
- *   scratch array (with that device current) and may load the library's
- *   device code there; make that first call before any stream capture.
+ *   scratch array and the device's L2 size (with that device current) and
+ *   may load the library's device code there; make that first call before
+ *   any stream capture.  The address is kept for the life of the process:
+ *   after cudaDeviceReset on a device, which unloads the library's device
+ *   code there, this call must not be used on that device again.
  * Sharing: every call, on every stream, uses the same scratch array and it
  *   keeps the last call's contents.  Calls that overlap on the device race
  *   with each other and give wrong results: serialise them (one stream, or
- *   events).  Nothing needs clearing between calls, because every word of the
- *   scratch that a call reads is first written by that call.  The record is
- *   not readable through the handle functions; use out_norm and
- *   out_nonfinite_flag.
+ *   events).  Nothing needs clearing between calls: every partial sum a call
+ *   reads is first written by that call; only the record's call counter is
+ *   carried over from call to call.  The record is not readable through the
+ *   handle functions; use out_norm and out_nonfinite_flag.
  * Returns GCLIP_OK; GCLIP_ERR_INVALID_ARG (bad dtype, negative numel, NULL or
  *   misaligned grads with numel > 0, bad max_norm / inv_scale);
  *   GCLIP_ERR_TOO_LARGE; GCLIP_ERR_CUDA (no current device, the scratch could
  *   not be located, or a launch failed).  Allocates nothing. */
 #define GCLIP_NOALLOC_MAX_CHUNKS 65536
-#define GCLIP_NOALLOC_SCRATCH_BYTES (GCLIP_NOALLOC_MAX_CHUNKS * 8 + 256)
+#define GCLIP_NOALLOC_SCRATCH_BYTES (GCLIP_NOALLOC_MAX_CHUNKS * 16 + 256)
 int clip_grad_norm_flat_noalloc(void *grads, int64_t numel, int32_t dtype,
                                 float max_norm, float inv_scale,
                                 float *out_norm, int32_t *out_nonfinite_flag,

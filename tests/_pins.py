@@ -193,6 +193,25 @@ def pin_closed_form_constant(o):
     assert abs(r.norm - 3 * math.sqrt(7)) <= 1e-15 * r.norm
 
 
+def pin_closed_form_tiny_magnitudes(o):
+    """||a * 1_n|| = |a| sqrt(n) where the squares lie far below fp32's range:
+    a = 2^-80 (fp32), 2^-140 (an fp32 subnormal), 2^-100 (bf16), and fp16
+    ones unscaled by 2^-100.  Every value is a power of two, so the norm and
+    the clipped outputs are exact; the clip at half the norm halves them
+    (and the fp16 result, 2^-102, is below fp16's range: +0)."""
+    cases = [(2.0 ** -80, 1024, "f32", 1.0, 2.0 ** -75, 2.0 ** -81),
+             (2.0 ** -140, 4096, "f32", 1.0, 2.0 ** -134, 2.0 ** -141),
+             (-(2.0 ** -100), 16, "bf16", 1.0, 2.0 ** -98, -(2.0 ** -101)),
+             (0.5, 256, "f16", 2.0 ** -100, 2.0 ** -97, 0.0)]
+    for a, n, dt, inv, norm, out in cases:
+        x = make(np.full(n, a), dt)
+        _, r = o.clip([x], 1.0, inv)
+        assert r.norm == norm and r.decision == PASS, (a, dt, r.norm)
+        outs, r = o.clip([x], norm / 2, inv)
+        assert r.decision == CLIP and r.coef == 0.5, (a, dt)
+        assert np.all(as_float64(outs[0]) == out), (a, dt)
+
+
 def pin_nonfinite(o):
     """NaN or +-inf raises the flag and leaves every gradient as it was
     (glossary page: a nonfinite value needs diagnosis and a stopped update)."""

@@ -14,3 +14,11 @@ def test_oracle_all_cores_runs_one_replica_per_core():
 def test_algorithmic_bytes():
     assert bench.algorithmic_bytes(10, 4, "write") == 120
     assert bench.algorithmic_bytes(10, 2, "read") == 20
+
+
+def test_pool_leaves_at_least_four_timed_runs():
+    assert bench.pool_size(32, 20) == 5            # the driver's short run: 4 runs
+    assert bench.pool_size(32, 3200) == 32
+    assert bench.pool_size(32, 3) == 1
+    for steps in range(4, 200):
+        assert -(-steps // bench.pool_size(32, steps)) >= 4

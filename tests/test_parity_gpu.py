@@ -14,7 +14,7 @@ from workloads import WORKLOADS, make_gradset
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["split", "persistent", "split_tma", "persistent_tma", "split_wave"]
+VARIANTS = ["split", "persistent", "split_tma", "persistent_tma", "split_wave", "three_kernel"]
 TD = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -79,7 +79,7 @@ def test_andrea120m(variant, name):
         assert res["worst_ulp"]["f16"] == 0
 
 
-@pytest.mark.parametrize("variant", ["persistent", "split_tma"])
+@pytest.mark.parametrize("variant", ["split", "persistent", "split_tma", "three_kernel"])
 def test_andrea1p2b(variant):
     gs = make_gradset("andrea1p2b", device=dev())
     before = host_copies(gs.tensors)
@@ -244,7 +244,7 @@ def test_rejects_host_memory_descriptor():
 # -- determinism ----------------------------------------------------------------
 
 @pytest.mark.parametrize("pair", [("split", "persistent"), ("split_tma", "persistent_tma"),
-                                  ("split", "split_wave")])
+                                  ("split", "split_wave"), ("three_kernel", "three_kernel")])
 def test_bit_identical_runs_and_variants(pair):
     """100 runs alternating the two variants of one engine: the same norm,
     sum of squares and multiplier bit for bit, and the same outputs."""
@@ -288,15 +288,19 @@ def test_barrier_timeout_reports_and_writes_nothing(variant):
     with g.GradClipper(gs.tensors, variant=variant) as c:
         c.debug_barrier(1, 20_000_000)     # one arrival that never comes; 20 ms
         c.clip_(1e-3)
+        status = c.last_status()
         rec = c.result()
         assert rec["status"] == g.GCLIP_STATUS_TIMEOUT
+        assert int(status.item()) == g.GCLIP_STATUS_TIMEOUT
         for b, t in zip(before, gs.tensors):
             assert np.array_equal(storage_bits(b), storage_bits(to_oracle(t)))
         c.debug_barrier(0)
         c.reset()
         c.clip_(1e-3)
+        status = c.last_status()
         rec = c.result()
         assert rec["status"] == g.GCLIP_STATUS_OK
+        assert int(status.item()) == g.GCLIP_STATUS_OK
         assert rec["decision"] == g.GCLIP_DECISION_CLIP
     rec["out_norm"], rec["out_flag"] = rec["norm"], rec["nonfinite"]
     compare(before, gs.tensors, rec, 1e-3, 1.0, "after-timeout")
@@ -366,7 +370,7 @@ def many_small(seed, n=20000, dt=torch.float32):
     return ts
 
 
-@pytest.mark.parametrize("variant", ["split", "persistent", "split_tma"])
+@pytest.mark.parametrize("variant", ["split", "persistent", "split_tma", "three_kernel"])
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
 def test_twenty_thousand_small_tensors(variant, dt):
     ts = many_small(5, dt=dt)
