@@ -269,11 +269,10 @@ __device__ __forceinline__ bool must_write(int decision, float chi, float clo) {
 // increasing order, then the fixed block tree; thread 0 writes the record.
 // An entry is one SumSq packed as float4 {big.hi, big.lo, tiny.hi, tiny.lo}.
 //
-// The decision is taken in double: S = big + tiny * 2^-2K is formed in double
-// (each float-float bin exactly, one rounding for the sum), norm = sqrt(S)
-// and max_norm / norm are IEEE double operations, and the multiplier
-// inv_scale * max_norm / norm is handed to the scaling pass as a float-float
-// pair so that each output is rounded once.
+// The decision (decide_write) is taken in float-float arithmetic, or in
+// double when the tiny bin is not empty, and the multiplier inv_scale *
+// max_norm / norm is handed to the scaling pass as a float-float pair so
+// that each output is rounded once.
 
 __device__ SumSq reduce_partials(const float4* partials, int64_t n, SumSq* red) {
   SumSq acc = {{0.f, 0.f}, {0.f, 0.f}};
@@ -293,41 +292,110 @@ __device__ SumSq reduce_partials(const float4* partials, int64_t n, SumSq* red) 
   return block_reduce(acc, red);
 }
 
+// Float-float steps of the decision, after Dekker ("A floating-point
+// technique for extending the available precision", 1971): products made
+// exact with a fused multiply-add; a square root and a quotient each taken
+// as the fp32 result plus one correction from the exactly computed
+// remainder, good to about 2^-46.  GB300 runs fp64 at a small fraction of
+// its fp32 rate, and one thread's dependent chain of double square root and
+// division sat on the critical path of every clip.
+
+__device__ __forceinline__ FF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return FF{p, __fmaf_rn(a, b, -p)};
+}
+
+// sqrt(a) for a normalized float-float a > 0 whose high part is normal.
+__device__ __forceinline__ FF ff_sqrt(FF a) {
+  const float s = __fsqrt_rn(a.hi);
+  const FF p = two_prod(s, s);
+  // a - s^2: a.hi - p.hi is exact (the two are within a factor of two)
+  const float r = __fadd_rn(__fsub_rn(__fsub_rn(a.hi, p.hi), p.lo), a.lo);
+  return ff_renorm(s, __fdiv_rn(r, __fmul_rn(2.0f, s)));
+}
+
+// m / n for a float m and a normalized float-float n > 0.
+__device__ __forceinline__ FF ff_div(float m, FF n) {
+  const float q = __fdiv_rn(m, n.hi);
+  // m - q * n.hi is exact for a correctly rounded q
+  const float r = __fsub_rn(__fmaf_rn(-q, n.hi, m), __fmul_rn(q, n.lo));
+  return ff_renorm(q, __fdiv_rn(r, n.hi));
+}
+
+__device__ __forceinline__ FF ff_mul(FF a, float b) {
+  const FF p = two_prod(a.hi, b);
+  return ff_renorm(p.hi, __fmaf_rn(a.lo, b, p.lo));
+}
+
 // The norm, flag, decision and multiplier from the two-bin sum of squares
 // (thread 0).  `tiny_exp` is the K of the call (the tiny bin holds squares
-// scaled by 2^2K).
+// scaled by 2^2K).  When the tiny bin is empty (the usual case) the sum is
+// the float-float big bin and everything is done in float-float: the norm
+// is compared with max_norm exactly as a float-float value, reported
+// rounded to fp32, and the multiplier inv_scale * max_norm / norm is handed
+// on as a float-float pair.  Otherwise the bins are combined and the same
+// steps taken in double.
 __device__ void decide_write(SumSq acc, float max_norm, float inv_scale, int tiny_exp,
                              clip_result_t* res, float* out_norm, int32_t* out_flag,
                              unsigned int calls) {
-  const double big = static_cast<double>(acc.big.hi) + static_cast<double>(acc.big.lo);
-  const double tiny = static_cast<double>(acc.tiny.hi) + static_cast<double>(acc.tiny.lo);
-  const double S = big + ldexp(tiny, -2 * tiny_exp);
-  const bool nonfinite = !isfinite(acc.big.hi) || !isfinite(acc.big.lo) ||
-                         !isfinite(acc.tiny.hi) || !isfinite(acc.tiny.lo) ||
-                         S > static_cast<double>(FLT_MAX);
-  const double norm = sqrt(S);
+  bool nonfinite;
   int decision;
-  float chi = 1.0f, clo = 0.0f;
-  if (nonfinite) {
-    decision = GCLIP_DECISION_SKIP;
-  } else if (norm > static_cast<double>(max_norm)) {
-    decision = GCLIP_DECISION_CLIP;
-    const double k = static_cast<double>(inv_scale) * (static_cast<double>(max_norm) / norm);
-    chi = __double2float_rn(k);
-    clo = __double2float_rn(k - static_cast<double>(chi));
+  float norm_f, s_hi, s_lo, chi = 1.0f, clo = 0.0f;
+  if (acc.tiny.hi == 0.0f && acc.tiny.lo == 0.0f) {
+    s_hi = acc.big.hi;
+    s_lo = acc.big.lo;
+    // S = s_hi + s_lo exactly; S > FLT_MAX only if s_hi is FLT_MAX and s_lo > 0
+    nonfinite = !isfinite(s_hi) || !isfinite(s_lo) || (s_hi == FLT_MAX && s_lo > 0.0f);
+    if (nonfinite) {
+      decision = GCLIP_DECISION_SKIP;
+      norm_f = __fsqrt_rn(s_hi);
+    } else if (s_hi == 0.0f) {
+      decision = GCLIP_DECISION_PASS;
+      norm_f = 0.0f;
+      chi = inv_scale;
+    } else {
+      // a non-zero big bin holds vectors whose sums are at least 2^-100
+      const FF n = ff_sqrt(acc.big);
+      norm_f = n.hi;
+      if (n.hi > max_norm || (n.hi == max_norm && n.lo > 0.0f)) {
+        decision = GCLIP_DECISION_CLIP;
+        const FF k = ff_mul(ff_div(max_norm, n), inv_scale);
+        chi = k.hi;
+        clo = k.lo;
+      } else {
+        decision = GCLIP_DECISION_PASS;
+        chi = inv_scale;
+      }
+    }
   } else {
-    decision = GCLIP_DECISION_PASS;
-    chi = inv_scale;
+    const double big = static_cast<double>(acc.big.hi) + static_cast<double>(acc.big.lo);
+    const double tiny = static_cast<double>(acc.tiny.hi) + static_cast<double>(acc.tiny.lo);
+    const double S = big + ldexp(tiny, -2 * tiny_exp);
+    nonfinite = !isfinite(acc.big.hi) || !isfinite(acc.big.lo) || !isfinite(acc.tiny.hi) ||
+                !isfinite(acc.tiny.lo) || S > static_cast<double>(FLT_MAX);
+    const double norm = sqrt(S);
+    if (nonfinite) {
+      decision = GCLIP_DECISION_SKIP;
+    } else if (norm > static_cast<double>(max_norm)) {
+      decision = GCLIP_DECISION_CLIP;
+      const double k = static_cast<double>(inv_scale) * (static_cast<double>(max_norm) / norm);
+      chi = __double2float_rn(k);
+      clo = __double2float_rn(k - static_cast<double>(chi));
+    } else {
+      decision = GCLIP_DECISION_PASS;
+      chi = inv_scale;
+    }
+    norm_f = __double2float_rn(norm);
+    s_hi = __double2float_rn(S);
+    s_lo = __double2float_rn(S - static_cast<double>(s_hi));
   }
-  const float norm_f = __double2float_rn(norm);
-  const float s_hi = __double2float_rn(S);
   res->norm = norm_f;
   res->nonfinite = nonfinite ? 1 : 0;
   res->decision = decision;
   res->coef_hi = chi;
   res->coef_lo = clo;
   res->sumsq_hi = s_hi;
-  res->sumsq_lo = __double2float_rn(S - static_cast<double>(s_hi));
+  res->sumsq_lo = s_lo;
   res->calls = calls + 1u;  // `calls`: the count read before the reduction
   if (out_norm) *out_norm = norm_f;
   if (out_flag) *out_flag = nonfinite ? 1 : 0;
