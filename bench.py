@@ -136,16 +136,18 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_from_profile(kernel: str):
+def traffic_from_profile(kernel: str, variant: str = ""):
     """DRAM bytes per launch from the committed ncu summary, if that summary
-    was taken on the current kernel source; else None."""
+    was taken on the current kernel source; else None.  An entry
+    "<kernel>@<variant>" (the kernel as that variant runs it) wins over the
+    plain kernel name."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(kernel)
+    e = d.get(f"{kernel}@{variant}") or d.get(kernel)
     if not e or e.get("source_digest") != source_digest():
         return None
     return e.get("dram_bytes_per_launch")
@@ -587,7 +589,7 @@ def run_gclip(args):
     peak = peaks.get("hbm_gbs") or 6800.0
     peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
     achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else 0.0
-    traffic = traffic_from_profile(kernel)
+    traffic = traffic_from_profile(kernel, args.variant)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
                 "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"

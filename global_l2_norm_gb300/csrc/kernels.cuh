@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kThreads) k_grad_norm_final(const float4* __re
 // entry point.  `clear` (may be NULL): two words zeroed by block 0 before
 // anything else (per-tensor clipping's write list).
 template <class Src>
-__global__ void __launch_bounds__(kThreads) k_chunk_sums(const Src src, float s, float st,
+__global__ void __launch_bounds__(kThreads, 5) k_chunk_sums(const Src src, float s, float st,
                                                          float4* __restrict__ partials,
                                                          unsigned int* clear, int resident) {
   __shared__ SumSq red[kWarps];
