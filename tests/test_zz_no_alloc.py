@@ -133,6 +133,35 @@ def test_noalloc_edge_cases():
     assert norm == 0.0 and flag == 0
 
 
+def test_noalloc_largest_buffer():
+    """Exactly GCLIP_NOALLOC_MAX_CHUNKS chunks (2 GiB of fp32, aligned start):
+    accepted, the norm against the oracle, outputs on a sample the oracle
+    computes one by one, and bit for bit against the three-kernel handle."""
+    g.build()
+    per = _abi.GCLIP_CHUNK_BYTES // 4
+    n = _abi.GCLIP_NOALLOC_MAX_CHUNKS * per
+    x = torch.empty(n, device="cuda")
+    assert x.data_ptr() % 16 == 0
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    x.normal_(0.0, 1e-4, generator=gen)
+    x[n // 2: n // 2 + 1000] *= 1e4
+    host = to_oracle(x)
+    three = x.clone()
+    norm, flag = noalloc(x, _abi.GCLIP_F32, 1.0, 1.0)
+    idx = np.concatenate([np.arange(0, 64), np.arange(n - 64, n), np.arange(n // 2, n // 2 + 64),
+                          np.random.default_rng(2).integers(0, n, 4096)])
+    slots, r = oracle.default().clip_sample([host], 1.0, 1.0, np.zeros(idx.size), idx)
+    assert flag == 0 and r.decision == oracle.CLIP
+    assert abs(norm - r.norm) <= 1e-5 * r.norm, (norm, r.norm)
+    got = x[torch.from_numpy(idx).cuda()].cpu().numpy()
+    want = (slots & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+    assert int(ulp_distance(oracle.OracleTensor(got, "f32"), oracle.OracleTensor(want, "f32")).max()) <= 2
+    del host
+    rec = handle(three, "three_kernel", 1.0, 1.0)
+    assert np.float32(rec["out_norm"]).view(np.int32) == np.float32(norm).view(np.int32)
+    assert torch.equal(three, x)
+
+
 def test_noalloc_rejects_oversized_and_bad_arguments():
     L = _abi.load()
     x = torch.ones(8, device="cuda")
