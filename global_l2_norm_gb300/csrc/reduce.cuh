@@ -479,6 +479,7 @@ struct NormArgs {
   int64_t keep_from;      // chunks from here on are read with evict_last
   int resident;           // the set fits in half of L2: the rest is read with evict_normal
   int prefetch;           // each block asks L2 for its next chunk ahead of its loads
+  int32_t* hint;          // mapped host word: 1 if this clip writes, else 0 (may be NULL)
 };
 
 // This block's chunk c: its share into `acc`, after a bulk L2 prefetch of
@@ -528,6 +529,11 @@ __device__ __forceinline__ bool norm_arrive(const NormArgs& a, SumSq bsum, SumSq
   final_reduce(a.block_sums, gridDim.x, a.max_norm, a.inv_scale, a.tiny_exp, a.res, a.out_norm,
                a.out_flag, red);
   if (threadIdx.x == 0) {
+    // For the host's choice of the next call's scaling launch (this thread
+    // wrote the record just now).
+    if (a.hint != nullptr)
+      *reinterpret_cast<volatile int32_t*>(a.hint) =
+          must_write(a.res->decision, a.res->coef_hi, a.res->coef_lo) ? 1 : 0;
     // No fence: the end of the kernel orders these stores and the record
     // before the dependent launch; the single-launch kernels fence before
     // they release the other blocks.

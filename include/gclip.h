@@ -63,7 +63,11 @@ extern "C" {
                                        ("ANDREA's three-kernel pipeline")
                                        in two launches: partial sums with
                                        the final reduction done by the last
-                                       block to finish, then the scaling   */
+                                       block to finish, then the scaling,
+                                       with one block per chunk after a
+                                       call that wrote and as the claiming
+                                       wave of SPLIT_WAVE after one that did
+                                       not (see clip_grad_norm)             */
 #define GCLIP_VARIANT_PERSISTENT 1  /* all three steps in one cooperative
                                        launch: the last block to finish
                                        reduces, the others wait for it on a
@@ -137,8 +141,9 @@ typedef struct gclip_handle *clip_handle_t;
  * the grad norm needs three kernels": embedding 8449x768 next to layer norm
  * [768]).  This call builds that fragment (chunk) table once, on the host,
  * uploads it, and allocates the per-chunk scratch of partial sums and the
- * result record on the current CUDA device.  It is the only call that
- * allocates.
+ * result record on the current CUDA device, and one small pinned host word
+ * (the write hint of GCLIP_VARIANT_SPLIT).  It is the only call that
+ * allocates, apart from the attach calls.
  *
  * descs, n_tensors: host array of the gradient tensors, in the order their
  *   squares are summed; copied, so the array may be freed on return.  The
@@ -184,6 +189,15 @@ int clip_create(const clip_tensor_desc_t *descs, int32_t n_tensors,
  * accurate to about one fp32 ulp for gradients of any magnitude down to the
  * smallest fp32 values (below about 1e-40, where the fp32 norm itself is
  * subnormal, it is accurate to an fp32 ulp of that range).
+ *
+ * With GCLIP_VARIANT_SPLIT the shape of the scaling launch follows the
+ * decision of the last call on this handle that has completed when this one
+ * is enqueued: the norm pass's last block writes whether it will write into
+ * a small pinned host word (allocated by clip_create), which this call reads
+ * without waiting.  After a clip that wrote, one block per chunk; after one
+ * that wrote nothing, one resident wave of blocks (few blocks to retire).
+ * Both give the same results bit for bit; a wrong guess costs time only.  A
+ * call captured in a CUDA graph keeps the shape chosen at capture.
  *
  * max_norm: threshold c, finite and > 0.  inv_scale: finite and > 0.
  * out_norm: device float, may be NULL; receives the norm (fp32).

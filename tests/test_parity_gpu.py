@@ -265,6 +265,24 @@ def test_bit_identical_runs_and_variants(pair):
         assert np.array_equal(a, b)
 
 
+def test_split_scaling_follows_the_last_decision():
+    """SPLIT chooses its scaling launch (one block per chunk, or one claiming
+    wave) from the decision of the last call that has completed on the
+    handle.  Alternating clipping and no-write calls makes every guess wrong,
+    repeated decisions make them right; every call matches the oracle."""
+    gs = make_gradset("andrea14m", device=dev())          # norm ~0.378
+    pristine = clone_all(gs.tensors)
+    with g.GradClipper(gs.tensors) as c:
+        for i, m in enumerate([1.0, 0.1, 1.0, 0.1, 0.1, 1.0, 1.0, 0.1, 0.1]):
+            restore(gs.tensors, pristine)
+            before = host_copies(gs.tensors)
+            c.clip_(m, 1.0)
+            rec = c.result()
+            rec["out_norm"], rec["out_flag"] = float(c.norm.item()), int(c.flag.item())
+            res = compare(before, gs.tensors, rec, m, 1.0, f"call {i}")
+            assert res["oracle"].decision == (oracle.CLIP if m < 0.3 else oracle.PASS)
+
+
 def test_clip_twice_is_stable():
     """After a clip the norm is max_norm: a second call sees norm ~= 1."""
     gs = make_gradset("andrea14m", device=dev())
