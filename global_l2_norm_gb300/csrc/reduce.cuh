@@ -89,9 +89,16 @@ __device__ __forceinline__ FF warp_reduce(FF v, int width) {
   return v;
 }
 
+// The tiny bin is usually +0 in every thread (it only ever adds squares):
+// a warp whose tiny bins are all +0 skips their tree, whose result would be
+// +0 anyway.
+__device__ __forceinline__ bool any_tiny(const FF& t) {
+  return __any_sync(0xffffffffu, t.hi != 0.f || t.lo != 0.f);
+}
+
 __device__ __forceinline__ SumSq block_reduce(SumSq v, SumSq* red) {
   v.big = warp_reduce(v.big, 32);
-  v.tiny = warp_reduce(v.tiny, 32);
+  if (any_tiny(v.tiny)) v.tiny = warp_reduce(v.tiny, 32);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = v;
   __syncthreads();
@@ -99,7 +106,7 @@ __device__ __forceinline__ SumSq block_reduce(SumSq v, SumSq* red) {
   if (warp == 0) {
     if (lane < kWarps) r = red[lane];
     r.big = warp_reduce(r.big, kWarps);
-    r.tiny = warp_reduce(r.tiny, kWarps);
+    if (any_tiny(r.tiny)) r.tiny = warp_reduce(r.tiny, kWarps);
   }
   __syncthreads();
   return r;
