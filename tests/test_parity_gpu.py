@@ -350,6 +350,29 @@ def test_captured_in_a_cuda_graph(variant):
             compare(before, gs.tensors, rec, 1.0, 0.5, "graph")
 
 
+def test_graph_captured_after_a_no_write_call():
+    """A SPLIT clip captured right after a call that wrote nothing keeps the
+    claiming-wave scaling it chose then; replayed on gradients that clip, it
+    must still write every element correctly."""
+    gs = make_gradset("andrea14m", device=dev())          # norm ~0.378: no write at 1.0
+    pristine = clone_all(gs.tensors)
+    before = host_copies(gs.tensors)
+    with g.GradClipper(gs.tensors) as c:
+        c.clip_(1.0)
+        assert c.result()["decision"] == g.GCLIP_DECISION_PASS   # synchronises: the hint is set
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            c.clip_(0.1, 0.5)
+        for _ in range(2):
+            restore(gs.tensors, pristine)
+            graph.replay()
+            torch.cuda.synchronize()
+            rec = c.result()
+            rec["out_norm"], rec["out_flag"] = float(c.norm.item()), int(c.flag.item())
+            res = compare(before, gs.tensors, rec, 0.1, 0.5, "graph-after-pass")
+            assert res["oracle"].decision == oracle.CLIP
+
+
 # -- accuracy of the norm -------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["tiny", "andrea14m", "andrea120m", "andrea120m_fp16",
