@@ -12,17 +12,20 @@
 // the job into a partial-sum kernel (one block per fragment of a tensor,
 // results into a small scratch buffer), a final kernel that reduces the
 // scratch to one scalar and takes its square root, and a scaling kernel.
-// This file keeps that split as one variant and adds a single-launch variant
-// in which the last block to finish its partial sums does the final
-// reduction and releases the others to scale (the page's heading "Why three
-// kernels and not one?" has no body, so the page gives no reason against it).
+// This file keeps that pipeline as written (GCLIP_VARIANT_THREE_KERNEL), runs
+// it by default in two launches (the last block of the partial-sum kernel
+// does the final reduction), and adds a single-launch variant in which the
+// last block to finish its partial sums reduces and releases the others to
+// scale (the page's heading "Why three kernels and not one?" has no body, so
+// the page gives no reason against it).
 //
-// Both variants share every piece of arithmetic: the per-chunk sum (a fixed
-// mapping of elements to the 256 threads of a block, fp32 squares, a
-// float-float accumulator, a fixed shuffle tree) and the final reduction (a
-// fixed strided order over chunks, the same tree), so the norm and the output
-// are bit-identical between variants and from run to run.  The work is a
-// streaming reduction bounded by HBM bandwidth; no tensor cores are used.
+// The variants share every piece of arithmetic: the sums of squares (a fixed
+// mapping of elements to the 256 threads of a block, fp32 squares into two
+// float-float bins, a fixed shuffle tree) and the final reduction (a fixed
+// strided order over the partial sums, the same tree, the decision), so the
+// norm is bit-identical from run to run, and between the variants that cut
+// the partial sums the same way.  The work is a streaming reduction bounded
+// by HBM bandwidth; no tensor cores are used.
 //
 // Layout: common.cuh (float-float arithmetic, element formats, memory
 // policies), reduce.cuh (chunk sums, block tree, final reduction, norm pass),

@@ -1,6 +1,7 @@
 // reduce.cuh -- the arithmetic of the norm: per-thread sums of squares of a
 // chunk (plain, or with the last microbatch added in), the fixed block tree,
-// the scaling of a chunk, the final reduction with the decision in double,
+// the scaling of a chunk, the final reduction with the decision in
+// float-float (double when the tiny bin is not empty),
 // and the norm pass shared by the register-engine variants.
 // Included by gclip.cu only.
 #pragma once

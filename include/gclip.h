@@ -183,9 +183,10 @@ int clip_create(const clip_tensor_desc_t *descs, int32_t n_tensors,
  * float-float accumulators, so the norm is bit-identical from run to run and
  * between the SPLIT, SPLIT_WAVE and PERSISTENT variants (the two TMA variants
  * share another fixed order, THREE_KERNEL a third).  Squares are fp32, in two
- * bins: elements whose unscaled magnitude is below 2^-60 are summed scaled
- * by a power of two, so that their squares neither underflow nor lose
- * precision; the bins are combined in double.  The norm is therefore
+ * bins: a 16-byte vector whose fp32 sum of unscaled squares is below 2^-100
+ * (every element's unscaled magnitude below 2^-50) is summed again scaled by
+ * a power of two, so that its squares neither underflow nor lose precision;
+ * the bins are combined in double.  The norm is therefore
  * accurate to about one fp32 ulp for gradients of any magnitude down to the
  * smallest fp32 values (below about 1e-40, where the fp32 norm itself is
  * subnormal, it is accurate to an fp32 ulp of that range).
