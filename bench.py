@@ -123,16 +123,47 @@ def aggregate(elapsed_ms: float, units: float, world: int, reduce_max=None):
     return units * world / (t / 1e3), t
 
 
-def source_digest() -> str:
-    """Digest of the library's sources: every file under csrc/ and the C ABI
-    header, whose constants the kernels are compiled with."""
+def strip_comments(text: str) -> str:
+    """C/C++ source without its comments and with whitespace collapsed, so
+    that a change of wording alone leaves the digest of the code unchanged.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_digest(read=None) -> str:
+    """Digest of the library's code: every file under csrc/ and the C ABI
+    header (whose constants the kernels are compiled with), comments and
+    whitespace left out.  `read(relative_path)` may supply the files' text
+    (for another revision); by default they are read from this tree."""
+    if read is None:
+        def read(rel):
+            with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+                return fh.read()
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "global_l2_norm_gb300", "csrc")
-    files = [os.path.join(d, f) for f in sorted(os.listdir(d))]
-    files.append(os.path.join(ROOT, "include", "gclip.h"))
-    for path in files:
-        with open(path, "rb") as fh:
-            h.update(os.path.basename(path).encode() + b"\0" + fh.read())
+    d = os.path.join("global_l2_norm_gb300", "csrc")
+    files = [os.path.join(d, f) for f in sorted(os.listdir(os.path.join(ROOT, d)))]
+    files.append(os.path.join("include", "gclip.h"))
+    for rel in files:
+        h.update(os.path.basename(rel).encode() + b"\0" + strip_comments(read(rel)).encode())
     return h.hexdigest()[:16]
 
 

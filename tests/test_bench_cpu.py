@@ -22,3 +22,10 @@ def test_pool_leaves_at_least_four_timed_runs():
     assert bench.pool_size(32, 3) == 1
     for steps in range(4, 200):
         assert -(-steps // bench.pool_size(32, steps)) >= 4
+
+
+def test_code_digest_ignores_comments_only():
+    src = 'int a = 1; // note\n/* block\n note */ const char* s = "//kept"; char c = \'/\';\n'
+    assert bench.strip_comments(src) == 'int a = 1; const char* s = "//kept"; char c = \'/\';'
+    assert bench.strip_comments("x = 1;   // one\n") == bench.strip_comments("x = 1;\n")
+    assert bench.strip_comments("x = 1;") != bench.strip_comments("x = 2;")
