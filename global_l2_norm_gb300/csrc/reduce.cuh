@@ -349,11 +349,13 @@ __device__ void decide_write(SumSq acc, float max_norm, float inv_scale, int tin
   bool nonfinite;
   int decision;
   float norm_f, s_hi, s_lo, chi = 1.0f, clo = 0.0f;
-  if (acc.tiny.hi == 0.0f && acc.tiny.lo == 0.0f) {
+  // Float-float unless the tiny bin holds something or the sum is within
+  // 2^8 of fp32's range (where the square root rounds to 2^64 and its exact
+  // square would overflow); those cases take the double path.
+  if (acc.tiny.hi == 0.0f && acc.tiny.lo == 0.0f && !(acc.big.hi > 0x1p120f)) {
     s_hi = acc.big.hi;
     s_lo = acc.big.lo;
-    // S = s_hi + s_lo exactly; S > FLT_MAX only if s_hi is FLT_MAX and s_lo > 0
-    nonfinite = !isfinite(s_hi) || !isfinite(s_lo) || (s_hi == FLT_MAX && s_lo > 0.0f);
+    nonfinite = !isfinite(s_hi) || !isfinite(s_lo);  // finite and below 2^120 here: S < FLT_MAX
     if (nonfinite) {
       decision = GCLIP_DECISION_SKIP;
       norm_f = __fsqrt_rn(s_hi);

@@ -186,6 +186,28 @@ def test_overflow_counts_as_nonfinite(variant):
     compare(before, [x], rec, 1.0, 1.0, "overflow")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_sum_of_squares_exactly_at_flt_max(variant):
+    """A set whose fp32 sum of squares rounds to exactly FLT_MAX: (2^64 (1 -
+    2^-24))^2 rounds to 2^128 (1 - 2^-23), plus (2^52)^2 is FLT_MAX.  The sum
+    is finite on the device, so the norm must be sqrt(FLT_MAX) and the clip
+    must scale, not produce a NaN (the exact sum lies one ulp above FLT_MAX,
+    inside the band around that threshold where the device's fp32 sum and
+    the oracle's exact one may decide differently, so this case is checked
+    for consistency rather than against the oracle)."""
+    x = torch.tensor([2.0 ** 64 * (1 - 2.0 ** -24), 2.0 ** 52, 0.0, 0.0], device=dev())
+    assert x.data_ptr() % 16 == 0
+    orig = x.double().cpu()
+    rec = gpu_clip([x], 1.0, 1.0, variant)
+    norm = float(np.float32(math.sqrt(float(np.finfo(np.float32).max))))
+    assert rec["nonfinite"] == 0 and rec["decision"] == g.GCLIP_DECISION_CLIP, rec
+    assert rec["norm"] == norm, (rec["norm"], norm)
+    want = (orig / math.sqrt(float(np.finfo(np.float32).max))).float()
+    got = x.cpu()
+    d = ulp_distance(OracleTensor(got.numpy(), "f32"), OracleTensor(want.numpy(), "f32"))
+    assert int(d.max()) <= 2, (got, want)
+
+
 def test_largest_tensor_64bit_offsets():
     """One fp16 tensor of 2^31 + 37 elements (4.3 GB): chunk addresses past
     2^32 bytes; the norm against the oracle, outputs on a sample (both ends
