@@ -167,9 +167,10 @@ def source_digest(read=None) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_from_profile(kernel: str, variant: str = ""):
+def traffic_from_profile(kernel: str, variant: str = "", workload: str = "andrea120m"):
     """DRAM bytes per launch from the committed ncu summary, if that summary
-    was taken on the current kernel source; else None.  An entry
+    was taken on the current kernel source and on this workload (an entry
+    that names none was taken on andrea120m); else None.  An entry
     "<kernel>@<variant>" (the kernel as that variant runs it) wins over the
     plain kernel name."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -180,6 +181,8 @@ def traffic_from_profile(kernel: str, variant: str = ""):
         return None
     e = d.get(f"{kernel}@{variant}") or d.get(kernel)
     if not e or e.get("source_digest") != source_digest():
+        return None
+    if e.get("workload", "andrea120m") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -620,7 +623,7 @@ def run_gclip(args):
     peak = peaks.get("hbm_gbs") or 6800.0
     peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
     achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else 0.0
-    traffic = traffic_from_profile(kernel, args.variant)
+    traffic = traffic_from_profile(kernel, args.variant, args.workload)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
                 "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"

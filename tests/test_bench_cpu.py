@@ -29,3 +29,24 @@ def test_code_digest_ignores_comments_only():
     assert bench.strip_comments(src) == 'int a = 1; const char* s = "//kept"; char c = \'/\';'
     assert bench.strip_comments("x = 1;   // one\n") == bench.strip_comments("x = 1;\n")
     assert bench.strip_comments("x = 1;") != bench.strip_comments("x = 2;")
+
+
+def test_traffic_applies_only_to_its_workload(tmp_path, monkeypatch):
+    import json
+    import os
+    os.makedirs(tmp_path / "profiles")
+    digest = bench.source_digest()
+    table = {"k_grad_norm_partial": {"dram_bytes_per_launch": 7, "source_digest": digest},
+             "k_to_f32": {"dram_bytes_per_launch": 9, "source_digest": digest,
+                          "workload": "andrea120m_fp16"},
+             "k_grad_scale": {"dram_bytes_per_launch": 5, "source_digest": "0" * 16}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(table))
+    real_root = bench.ROOT
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_digest", lambda read=None: digest)
+    assert bench.traffic_from_profile("k_grad_norm_partial", "split", "andrea120m") == 7
+    assert bench.traffic_from_profile("k_grad_norm_partial", "split", "andrea120m_fp16_inf") is None
+    assert bench.traffic_from_profile("k_to_f32", "split", "andrea120m_fp16") == 9
+    assert bench.traffic_from_profile("k_to_f32", "split", "andrea120m") is None
+    assert bench.traffic_from_profile("k_grad_scale", "split", "andrea120m") is None  # stale
+    assert real_root != str(tmp_path)
