@@ -609,9 +609,13 @@ def run_gclip(args):
         k_ms, k_bytes = shares[kernel]
     else:
         tma = args.variant.endswith("tma")
+        # split: one early-loading block per chunk after a clip that wrote,
+        # the claiming wave after one that did not (the library's choice)
+        scale = ("k_scale_tma" if tma else
+                 "k_grad_scale_wave" if args.variant == "split_wave" or not writes else
+                 "k_grad_scale_early")
         shares = {("k_norm_tma" if tma else "k_grad_norm_partial"): (seg_ms[0], w.numel * w.elem_bytes),
-                  ("k_scale_tma" if tma else "k_grad_scale_wave" if args.variant == "split_wave"
-                   else "k_grad_scale"): (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
+                  scale: (seg_ms[2], nbytes - w.numel * w.elem_bytes)}
         kernel = max(shares, key=lambda k: shares[k][0])
         k_ms, k_bytes = shares[kernel]
     peaks = {}

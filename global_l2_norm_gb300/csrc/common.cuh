@@ -313,6 +313,15 @@ struct HintMem {
                  : "l"(p), "l"(pol));
     return v;
   }
+  // Served by L2 even where L1 holds the line: for loads issued before the
+  // kernel's own griddepcontrol.wait (k_grad_scale_early).
+  __device__ static __forceinline__ uint4 ld_l2(const uint4* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+  }
   __device__ static __forceinline__ uint4 ld_norm(const uint4* p, uint64_t pol) { return ld(p, pol); }
   __device__ static __forceinline__ uint4 ld_scale(const uint4* p, uint64_t pol) { return ld(p, pol); }
   __device__ static __forceinline__ void st_scale(uint4* p, uint4 v, uint64_t pol) {

@@ -299,7 +299,13 @@ namespace {
 // chunk, and when everything is, one block per chunk is 0.7% faster.  Both
 // kernels give the same results bit for bit, so a wrong guess costs time
 // only.
-cudaError_t launch_scale(clip_handle_t h, cudaStream_t s, bool pdl) {
+//
+// `after_norm_pass`: the norm pass was k_grad_norm_partial, so one block per
+// chunk may be k_grad_scale_early, whose first wave loads its chunks before
+// the decision is out (measured on GB300, ANDREA-120M: a writing clip 161.0
+// -> 159.7 us, fp16 81.9 -> 81.0, tiny 7.4 -> 6.7; a no-write clip after a
+// writing one costs the same as before).
+cudaError_t launch_scale(clip_handle_t h, cudaStream_t s, bool pdl, bool after_norm_pass = false) {
   const clip_chunk_t* chunks = h->d_chunks;
   int64_t nc = h->n_chunks;
   const clip_result_t* cres = h->d_result;
@@ -311,6 +317,13 @@ cudaError_t launch_scale(clip_handle_t h, cudaStream_t s, bool pdl) {
     void* args[] = {&chunks, &nc, &cres, &work};
     return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale_wave),
                       static_cast<unsigned int>(h->grid_wave), s, args, pdl);
+  }
+  if (after_norm_pass) {
+    // the first resident wave of one-chunk scaling blocks
+    unsigned int n_early = static_cast<unsigned int>(h->grid_wave);
+    void* args[] = {&chunks, &nc, &cres, &n_early};
+    return launch_pdl(reinterpret_cast<const void*>(gclip::k_grad_scale_early),
+                      static_cast<unsigned int>(nc), s, args, pdl);
   }
   gclip::TableChunks src{chunks};
   void* args[] = {&src, &nc, &cres};
@@ -373,7 +386,7 @@ int enqueue(clip_handle_t h, float max_norm, float inv_scale, float* out_norm,
                      static_cast<unsigned int>(h->grid_persistent), s, a1, pdl);
     mark(1);
     mark(2);
-    if (e == cudaSuccess) e = launch_scale(h, s, pdl);
+    if (e == cudaSuccess) e = launch_scale(h, s, pdl, true);
   } else if (h->variant == GCLIP_VARIANT_SPLIT_TMA) {
     gclip::NormArgs a = norm_args(h, h->grid_tma, max_norm, inv_scale, out_norm, out_flag, 0);
     void* a1[] = {&a};

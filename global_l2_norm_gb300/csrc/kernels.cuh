@@ -17,12 +17,15 @@ namespace gclip {
 __global__ void __launch_bounds__(kThreads, 4) k_grad_norm_partial(const NormArgs a) {
   __shared__ SumSq red[kWarps];
   __shared__ int s_flag;
-  // Let the dependent scaling launch be scheduled while this grid runs.
-  asm volatile("griddepcontrol.launch_dependents;");
   // Launched as a dependent of whatever the stream ran before (it may be the
   // kernel that produced the gradients): wait for it to finish before
   // reading any gradient.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Only then let the dependent scaling launch be scheduled while this grid
+  // runs: its blocks start after every block of this grid has passed the
+  // wait above, so the gradients they load before their own wait
+  // (k_grad_scale_early) are the producer's final values.
+  asm volatile("griddepcontrol.launch_dependents;");
   const SumSq bsum = block_norm_pass(a, red);
   norm_arrive(a, bsum, red, &s_flag);
 }
@@ -77,6 +80,83 @@ __global__ void __launch_bounds__(kThreads) k_grad_scale(const Src src, int64_t 
   // Highest chunks first: the norm pass read them last and kept them in L2.
   const clip_chunk_t c = src[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
   chunk_scale<HintMem>(c, chi, clo, policy_evict_first());
+}
+
+// The scaling pass of GCLIP_VARIANT_SPLIT after k_grad_norm_partial, one
+// block per chunk (highest first, as k_grad_scale): blocks of the first
+// resident wave (blockIdx.x < n_early) load their chunk's vectors before the
+// decision is out, overlapping the norm pass's last blocks and its final
+// reduction; later blocks start after the decision and read the record first,
+// so that a clip that writes nothing loads at most that first wave.  Safe
+// only after a norm pass that triggers its dependents after its own
+// griddepcontrol.wait and writes no gradient (not after the accumulation
+// epilogue).  A chunk's aligned body is at most kUnroll vectors per thread,
+// so the early loads cover it; the head and tail elements are read after the
+// wait.  The same element-wise arithmetic as k_grad_scale.
+static_assert(GCLIP_CHUNK_BYTES == kUnroll * kThreads * 16,
+              "one round of kUnroll vectors per thread covers a chunk's body");
+
+template <int DT>
+__device__ __forceinline__ void scale_loaded(const Span& sp, const uint4 (&buf)[kUnroll], float chi,
+                                             float clo, uint64_t pol) {
+  uint4* v = reinterpret_cast<uint4*>(sp.body);
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const uint32_t i = threadIdx.x + u * kThreads;
+    if (i < sp.nvec) HintMem::st_scale(v + i, Fmt<DT>::scale(buf[u], chi, clo), pol);
+  }
+  constexpr uint32_t B = Fmt<DT>::kBytes;
+  if (threadIdx.x < sp.head) {
+    const uint64_t a = sp.addr + threadIdx.x * B;
+    Fmt<DT>::store1(a, Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(a), chi, clo));
+  }
+  if (threadIdx.x < sp.ntail) {
+    const uint64_t a = sp.addr + static_cast<uint64_t>(sp.tail_start + threadIdx.x) * B;
+    Fmt<DT>::store1(a, Fmt<GCLIP_F32>::scale1(Fmt<DT>::load1(a), chi, clo));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_grad_scale_early(const clip_chunk_t* __restrict__ chunks,
+                                                               int64_t n_chunks,
+                                                               const clip_result_t* res,
+                                                               unsigned int n_early) {
+  const bool early = blockIdx.x < n_early;
+  int decision = GCLIP_DECISION_SKIP;
+  float chi = 1.0f, clo = 0.0f;
+  if (!early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    decision = res->decision;
+    chi = res->coef_hi;
+    clo = res->coef_lo;
+    if (!must_write(decision, chi, clo)) return;
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
+  const clip_chunk_t c = chunks[n_chunks - 1 - static_cast<int64_t>(blockIdx.x)];
+  const int dt = c.meta & 0xffu;
+  // fp16 and bf16 share the 2-byte layout
+  const Span sp = dt == GCLIP_F32 ? make_span<GCLIP_F32>(c.addr, c.numel)
+                                  : make_span<GCLIP_F16>(c.addr, c.numel);
+  const uint64_t pol = policy_evict_first();
+  const uint4* v = reinterpret_cast<const uint4*>(sp.body);
+  uint4 buf[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const uint32_t i = threadIdx.x + u * kThreads;
+    buf[u] = i < sp.nvec ? HintMem::ld_l2(v + i, pol) : make_uint4(0, 0, 0, 0);
+  }
+  if (early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    decision = res->decision;
+    chi = res->coef_hi;
+    clo = res->coef_lo;
+    if (!must_write(decision, chi, clo)) return;
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
+  switch (dt) {
+    case GCLIP_F32: scale_loaded<GCLIP_F32>(sp, buf, chi, clo, pol); break;
+    case GCLIP_F16: scale_loaded<GCLIP_F16>(sp, buf, chi, clo, pol); break;
+    default: scale_loaded<GCLIP_BF16>(sp, buf, chi, clo, pol); break;
+  }
 }
 
 // The scaling pass as one resident wave: block b scales chunk b (counted from

@@ -319,6 +319,32 @@ def test_clip_twice_is_stable():
     assert abs(second["norm"] - 1.0) < 1e-6
 
 
+@pytest.mark.parametrize("name", ["andrea14m", "andrea120m"])
+def test_back_to_back_writing_calls_see_each_other(name):
+    """Calls enqueued back to back with no host wait, each halving every
+    element (inv_scale 1/2, no clip): each call's scaling pass reads what the
+    previous call's scaling pass wrote, although its first blocks load before
+    its decision is out and the calls overlap through programmatic dependent
+    launch.  Power-of-two scaling of normal fp32 values is exact, so after k
+    calls every element is x / 2^k bit for bit, and the last call's norm is
+    the first call's / 2^(k-1) (sums of squares scale exactly by 4^-j)."""
+    gs = make_gradset(name, device=dev())
+    before = [t.clone() for t in gs.tensors]
+    with g.GradClipper([t.clone() for t in before], variant="split") as c1:
+        c1.clip_(1e30, 0.5)
+        first = c1.result()["norm"]
+    k = 6
+    with g.GradClipper(gs.tensors, variant="split") as c:
+        for _ in range(k):
+            c.clip_(1e30, 0.5)
+        torch.cuda.synchronize()
+        rec = c.result()
+    assert rec["decision"] == g.GCLIP_DECISION_PASS and rec["nonfinite"] == 0
+    for t, b in zip(gs.tensors, before):
+        assert torch.equal(t, b * 2.0 ** -k)
+    assert rec["norm"] == first * 2.0 ** -(k - 1), (rec["norm"], first)
+
+
 # -- the single-launch variant's bounded barrier --------------------------------
 
 @pytest.mark.parametrize("variant", ["persistent", "persistent_tma"])
