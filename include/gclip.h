@@ -79,7 +79,7 @@ extern "C" {
 #define GCLIP_VARIANT_SPLIT_WAVE 4  /* as SPLIT, with the scaling done by one
                                        resident wave of blocks that claim
                                        chunks from a counter: slower by
-                                       about 0.5% when every element is
+                                       about 1.5% when every element is
                                        written, faster when nothing is
                                        (few blocks to retire)               */
 #define GCLIP_VARIANT_THREE_KERNEL 5  /* the clipping page's pipeline as
@@ -195,8 +195,10 @@ int clip_create(const clip_tensor_desc_t *descs, int32_t n_tensors,
  * decision of the last call on this handle that has completed when this one
  * is enqueued: the norm pass's last block writes whether it will write into
  * a small pinned host word (allocated by clip_create), which this call reads
- * without waiting.  After a clip that wrote, one block per chunk; after one
- * that wrote nothing, one resident wave of blocks (few blocks to retire).
+ * without waiting.  After a clip that wrote, one block per chunk, of which
+ * the first resident wave loads its chunks while the norm pass finishes;
+ * after one that wrote nothing, one resident wave of blocks (few blocks to
+ * retire).
  * Both give the same results bit for bit; a wrong guess costs time only.  A
  * call captured in a CUDA graph keeps the shape chosen at capture.
  *
