@@ -17,6 +17,14 @@ namespace gclip {
 __global__ void __launch_bounds__(kThreads, 4) k_grad_norm_partial(const NormArgs a) {
   __shared__ SumSq red[kWarps];
   __shared__ int s_flag;
+  // Sets of up to four times L2: ask L2 for this block's first chunk while
+  // the previous kernel may still run.  Only a hint: L2 keeps device memory
+  // coherent, so whatever the producer writes later still reaches the loads
+  // below, which come after the wait.  Measured on GB300 (ANDREA-120M): fp32
+  // clip -1.0 us, fp16 -1.6, no write -0.4, 14M and tiny -0.2; the 4.9 GB
+  // set lost 0.2% and is left out.
+  if (threadIdx.x == 0 && (a.prefetch || a.resident) && blockIdx.x < a.n_chunks)
+    prefetch_chunk_l2(a.chunks[blockIdx.x]);
   // Launched as a dependent of whatever the stream ran before (it may be the
   // kernel that produced the gradients): wait for it to finish before
   // reading any gradient.

@@ -492,19 +492,23 @@ struct NormArgs {
   int32_t* hint;          // mapped host word: 1 if this clip writes, else 0 (may be NULL)
 };
 
+// One bulk request asking L2 for the aligned body of chunk `ch` (a hint: it
+// reads nothing into registers).
+__device__ __forceinline__ void prefetch_chunk_l2(const clip_chunk_t& ch) {
+  const uint32_t es = (ch.meta & 0xffu) == GCLIP_F32 ? 4u : 2u;
+  const uint32_t head = min(ch.numel, static_cast<uint32_t>(((16u - (ch.addr & 15u)) & 15u) / es));
+  const uint32_t bytes = (ch.numel - head) / (16u / es) * 16u;
+  if (bytes)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ch.addr + head * es), "r"(bytes)
+                 : "memory");
+}
+
 // This block's chunk c: its share into `acc`, after a bulk L2 prefetch of
 // the aligned body of its next chunk (when the set is prefetched).
 __device__ __forceinline__ void norm_chunk(const NormArgs& a, int64_t c, const clip_chunk_t& ch,
                                            SumSq& acc, uint64_t pol_first, uint64_t pol_last) {
-  if (a.prefetch && threadIdx.x == 0 && c + gridDim.x < a.n_chunks) {
-    const clip_chunk_t nx = a.chunks[c + gridDim.x];
-    const uint32_t es = (nx.meta & 0xffu) == GCLIP_F32 ? 4u : 2u;
-    const uint32_t head = min(nx.numel, static_cast<uint32_t>(((16u - (nx.addr & 15u)) & 15u) / es));
-    const uint32_t bytes = (nx.numel - head) / (16u / es) * 16u;
-    if (bytes)
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nx.addr + head * es), "r"(bytes)
-                   : "memory");
-  }
+  if (a.prefetch && threadIdx.x == 0 && c + gridDim.x < a.n_chunks)
+    prefetch_chunk_l2(a.chunks[c + gridDim.x]);
   chunk_accumulate<HintMem>(acc, ch, a.inv_scale, a.inv_scale_tiny,
                             c >= a.keep_from ? pol_last : pol_first);
 }
