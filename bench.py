@@ -640,6 +640,24 @@ def run_gclip(args):
         # lets `frac` exceed 1.
         roofline["dram_achieved"] = round(traffic / (k_ms / 1e3) / 1e9, 1)
         roofline["dram_frac"] = round(traffic / (k_ms / 1e3) / 1e9 / peak, 4)
+    # The split variants' other kernel, the norm pass, the same way (when it is
+    # not the dominant one): its algorithmic reads and, with the committed
+    # counters, its DRAM bytes (reads plus the previous clip's write-backs it
+    # absorbs) over its own event-timed launch.
+    norm_pass = None
+    if (not (args.per_tensor or args.to_f32 or args.accumulate) and args.variant.startswith("split")
+            and kernel != ("k_norm_tma" if args.variant.endswith("tma") else "k_grad_norm_partial")
+            and seg_ms[0] > 0):
+        nk = "k_norm_tma" if args.variant.endswith("tma") else "k_grad_norm_partial"
+        nb = w.numel * w.elem_bytes
+        norm_pass = {"kernel": nk, "launch_ms": round(seg_ms[0], 5), "algorithmic_bytes": nb,
+                     "achieved": round(nb / (seg_ms[0] / 1e3) / 1e9, 1),
+                     "frac": round(nb / (seg_ms[0] / 1e3) / 1e9 / peak, 4)}
+        nt = traffic_from_profile(nk, args.variant, args.workload)
+        norm_pass["traffic"] = nt
+        if nt:
+            norm_pass["dram_achieved"] = round(nt / (seg_ms[0] / 1e3) / 1e9, 1)
+            norm_pass["dram_frac"] = round(nt / (seg_ms[0] / 1e3) / 1e9 / peak, 4)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -749,6 +767,7 @@ def run_gclip(args):
                               "launch), the L2 not flushed between clips; a norm pass that "
                               "follows a writing clip also absorbs that clip's write-backs",
             "roofline": roofline,
+            "norm_pass": norm_pass,
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": args.steps * launches_per_step,
