@@ -296,7 +296,7 @@ namespace {
 // has completed on this handle decided to write nothing (the hint word, read
 // without synchronising; the calls enqueued since may not have run yet):
 // when nothing is written, the wave retires ~760 blocks instead of one per
-// chunk, and when everything is, one block per chunk is 0.7% faster.  Both
+// chunk, and when everything is, one block per chunk is 1.5% faster.  Both
 // kernels give the same results bit for bit, so a wrong guess costs time
 // only.
 //
