@@ -345,6 +345,52 @@ def test_back_to_back_writing_calls_see_each_other(name):
     assert rec["norm"] == first * 2.0 ** -(k - 1), (rec["norm"], first)
 
 
+@pytest.mark.parametrize("name", ["andrea120m", "andrea120m_fp16"])
+def test_pool_back_to_back_as_the_bench_runs_it(name):
+    """The bench's timed loop: a pool of distinct sets, each with its own
+    handle, clipped back to back on one stream with no host wait, so that
+    each clip's launches are chained to the previous clip's (another set) by
+    programmatic dependent launch.  Pass 1 writes (clip, or the fp16 unscale)
+    and matches the oracle set by set.  Passes 2 and 3 write nothing (pass 2
+    launches the one-block-per-chunk scaling pass, whose first wave loads
+    before the decision; pass 3 the claiming wave) and leave every bit as it
+    was.  Pass 4 clips again after a no-write call and matches the oracle."""
+    sets = [make_gradset(name, seed=1234 + 7 * k, device=dev(), flat=True) for k in range(4)]
+    clippers = [g.GradClipper(s.tensors, variant="split") for s in sets]
+
+    def run_pass(max_norm, inv_scale):
+        for c in clippers:
+            c.clip_(max_norm, inv_scale)
+        torch.cuda.synchronize()
+        recs = []
+        for c in clippers:
+            rec = c.result()
+            rec["out_norm"], rec["out_flag"] = float(c.norm.item()), int(c.flag.item())
+            recs.append(rec)
+        return recs
+
+    try:
+        before = [host_copies(s.tensors) for s in sets]
+        recs = run_pass(sets[0].max_norm, sets[0].inv_scale)
+        for k, (b, s, rec) in enumerate(zip(before, sets, recs)):
+            compare(b, s.tensors, rec, s.max_norm, s.inv_scale, f"{name} pass 1 set {k}")
+        after = [clone_all(s.tensors) for s in sets]
+        for p in (2, 3):
+            recs = run_pass(2.0, 1.0)
+            for k, (s, a, rec) in enumerate(zip(sets, after, recs)):
+                assert rec["decision"] == g.GCLIP_DECISION_PASS, (p, k, rec)
+                assert all(torch.equal(x, y) for x, y in zip(s.tensors, a)), (p, k)
+        before = [host_copies(s.tensors) for s in sets]
+        norms = [r["norm"] for r in recs]
+        recs = run_pass(0.5 * min(norms), 1.0)
+        for k, (b, s, rec) in enumerate(zip(before, sets, recs)):
+            res = compare(b, s.tensors, rec, 0.5 * min(norms), 1.0, f"{name} pass 4 set {k}")
+            assert res["oracle"].decision == oracle.CLIP
+    finally:
+        for c in clippers:
+            c.close()
+
+
 # -- the single-launch variant's bounded barrier --------------------------------
 
 @pytest.mark.parametrize("variant", ["persistent", "persistent_tma"])
