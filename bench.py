@@ -782,8 +782,9 @@ def run_gclip(args):
 
 def run_adamw(args):
     """The fused clip + AdamW step (clip_grad_norm_adamw) on the ANDREA set,
-    beside the unfused pipeline: this library's clip, then torch's fused
-    AdamW on the same tensors.  One JSON line."""
+    beside two unfused pipelines: this library's clip, then the same AdamW
+    kernel alone (clip_adamw_step), and this library's clip, then torch's
+    fused AdamW on the same tensors.  One JSON line."""
     import torch
 
     import global_l2_norm_gb300 as g
@@ -882,6 +883,16 @@ def run_adamw(args):
             done += P
         return total / done
 
+    # unfused within the library: the clip rewrites the gradients, then the
+    # AdamW kernel alone reads them (40 B per fp32 element against 32 fused)
+    def unfused_lib(i):
+        step_no[0] += 1
+        clippers[i].clip_(w.max_norm, w.inv_scale)
+        clippers[i].adamw_step_(step=step_no[0], **hp)
+
+    timed(unfused_lib, args.warmup, restore_grads)
+    unfused_lib_ms = timed(unfused_lib, args.steps, restore_grads)
+
     fused_graph = graph_of(lambda i: clippers[i].clip_adamw_(w.max_norm, w.inv_scale, step=7, **hp))
     timed_graph(fused_graph, args.warmup, lambda: None)
     fused_graph_ms = timed_graph(fused_graph, args.steps, lambda: None)
@@ -906,6 +917,7 @@ def run_adamw(args):
     fused_bytes = w.numel * (2 * es + 24)        # g read twice; w, m, v read and written
     # clip 3 * es; AdamW reads g, w, m, v and writes w, m, v
     unfused_bytes = w.numel * (3 * es + 4 + 12 + 12) if have_torch else None
+    unfused_lib_bytes = w.numel * (3 * es + es + 24)   # AdamW reads g in its own format
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -925,6 +937,12 @@ def run_adamw(args):
         "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(value / peak, 4)},
         "fused_graph_ms_per_step": round(fused_graph_ms, 5),
+        "unfused_library": {
+            "what": "clip_grad_norm (split), then clip_adamw_step (the same AdamW kernel alone, "
+                    "multiplier 1)",
+            "ms_per_step": round(unfused_lib_ms, 5), "bytes_per_step": unfused_lib_bytes,
+            "value": round(unfused_lib_bytes / (unfused_lib_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "speedup_of_fused": round(unfused_lib_ms / fused_ms, 3)},
         "unfused": None if unfused_ms is None else {
             "what": "clip_grad_norm (split) then torch.optim.AdamW(fused=True, capturable=True)",
             "ms_per_step": round(unfused_ms, 5),

@@ -210,6 +210,16 @@ class GradClipper:
             self.norm.data_ptr(), self.flag.data_ptr(), _stream_handle(stream, self.device)))
         return self.norm, self.flag
 
+    def adamw_step_(self, *, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                    eps: float = 1e-8, weight_decay: float = 0.0, step: int = 1,
+                    zero_grads: bool = False, stream=None) -> None:
+        """One AdamW step on the attached state with the gradients as they
+        are, no clip (see clip_adamw_step in include/gclip.h)."""
+        p = _abi.clip_adamw_params_t(float(lr), float(beta1), float(beta2), float(eps),
+                                     float(weight_decay), int(bool(zero_grads)))
+        check("clip_adamw_step", self._lib.clip_adamw_step(
+            self._h, ctypes.byref(p), int(step), _stream_handle(stream, self.device)))
+
     # -- configuration and inspection -----------------------------------
     def set_variant(self, variant) -> None:
         v = VARIANTS[variant] if isinstance(variant, str) else int(variant)

@@ -103,6 +103,7 @@ _SIGNATURES = {
     "clip_grad_norm_adamw": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float,
                                             ctypes.POINTER(clip_adamw_params_t), ctypes.c_int64,
                                             _P, _P, _P]),
+    "clip_adamw_step": (ctypes.c_int, [_P, ctypes.POINTER(clip_adamw_params_t), ctypes.c_int64, _P]),
     "clip_grad_norm_flat_noalloc": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_float, _P, _P, _P]),
 }

@@ -67,6 +67,7 @@ struct gclip_handle {
                              // block of the norm pass (G <= chunks)
   clip_result_t* d_result;
   SyncWords* d_sync;
+  clip_result_t* d_unit;     // a constant record: PASS, multiplier 1 (clip_adamw_step)
   int64_t* d_first;          // first chunk of each tensor, n_tensors + 1 entries
   clip_result_t* d_trec;     // per-tensor records of clip_grad_norm_per_tensor
   int64_t* d_wlist;          // chunks clip_grad_norm_per_tensor rewrites (n_chunks entries)
@@ -210,7 +211,8 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   const size_t off_trec = round_up(off_first + (nt + 1) * sizeof(int64_t), 256);
   const size_t off_wlist = round_up(off_trec + (nt ? nt : 1) * sizeof(clip_result_t), 256);
   const size_t off_wcount = round_up(off_wlist + (n ? n : 1) * sizeof(int64_t), 256);
-  const size_t total = round_up(off_wcount + 2 * sizeof(unsigned int), 256);
+  const size_t off_unit = round_up(off_wcount + 2 * sizeof(unsigned int), 256);
+  const size_t total = round_up(off_unit + sizeof(clip_result_t), 256);
   std::vector<int64_t> first(nt + 1, 0);
   {
     size_t c = 0;
@@ -235,6 +237,7 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
   h->d_trec = reinterpret_cast<clip_result_t*>(base + off_trec);
   h->d_wlist = reinterpret_cast<int64_t*>(base + off_wlist);
   h->d_wcount = reinterpret_cast<unsigned int*>(base + off_wcount);
+  h->d_unit = reinterpret_cast<clip_result_t*>(base + off_unit);
 
   int sms = 0, per_sm = 0, coop = 0, l2 = 0;
   e = cudaMemset(h->arena, 0, total);
@@ -242,6 +245,12 @@ extern "C" int clip_create(const clip_tensor_desc_t* descs, int32_t n_tensors, c
     e = cudaMemcpy(h->d_chunks, chunks.data(), n * sizeof(clip_chunk_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_first, first.data(), first.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    clip_result_t unit = {};
+    unit.decision = GCLIP_DECISION_PASS;
+    unit.coef_hi = 1.0f;
+    e = cudaMemcpy(h->d_unit, &unit, sizeof(unit), cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device);
@@ -709,19 +718,15 @@ extern "C" int clip_grad_norm_to_f32(clip_handle_t h, float max_norm, float inv_
                            reinterpret_cast<const void*>(gclip::k_to_f32), args);
 }
 
-extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
-                                    const clip_adamw_params_t* p, int64_t step, float* out_norm,
-                                    int32_t* out_nonfinite_flag, void* stream) {
-  if (h == nullptr || p == nullptr || h->d_states == nullptr || !valid_scalar(max_norm) ||
-      !valid_scalar(inv_scale) || step < 1)
-    return GCLIP_ERR_INVALID_ARG;
-  const bool ok = std::isfinite(p->lr) && p->lr >= 0.0f && std::isfinite(p->eps) && p->eps > 0.0f &&
-                  std::isfinite(p->weight_decay) && p->weight_decay >= 0.0f && p->beta1 >= 0.0f &&
-                  p->beta1 < 1.0f && p->beta2 >= 0.0f && p->beta2 < 1.0f;
-  if (!ok) return GCLIP_ERR_INVALID_ARG;
-  DeviceGuard guard(h->device);
-  if (!guard.ok) return GCLIP_ERR_CUDA;
-  gclip::AdamwArgs q;
+namespace {
+
+// The AdamW hyperparameters of step `step` as the kernel takes them; false
+// if one is out of range.
+bool adamw_args(const clip_adamw_params_t* p, int64_t step, gclip::AdamwArgs& q) {
+  const bool ok = step >= 1 && std::isfinite(p->lr) && p->lr >= 0.0f && std::isfinite(p->eps) &&
+                  p->eps > 0.0f && std::isfinite(p->weight_decay) && p->weight_decay >= 0.0f &&
+                  p->beta1 >= 0.0f && p->beta1 < 1.0f && p->beta2 >= 0.0f && p->beta2 < 1.0f;
+  if (!ok) return false;
   const double b1 = p->beta1, b2 = p->beta2;
   q.beta1 = p->beta1;
   q.beta2 = p->beta2;
@@ -733,6 +738,21 @@ extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_s
   q.lr = p->lr;
   q.decay = static_cast<float>(1.0 - static_cast<double>(p->lr) * p->weight_decay);
   q.zero_grads = p->zero_grads ? 1 : 0;
+  return true;
+}
+
+}  // namespace
+
+extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
+                                    const clip_adamw_params_t* p, int64_t step, float* out_norm,
+                                    int32_t* out_nonfinite_flag, void* stream) {
+  if (h == nullptr || p == nullptr || h->d_states == nullptr || !valid_scalar(max_norm) ||
+      !valid_scalar(inv_scale))
+    return GCLIP_ERR_INVALID_ARG;
+  gclip::AdamwArgs q;
+  if (!adamw_args(p, step, q)) return GCLIP_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
   int64_t nc = h->n_chunks;
   const clip_chunk_t* chunks = h->d_chunks;
   const gclip::TensorState* st = h->d_states;
@@ -741,6 +761,27 @@ extern "C" int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_s
   return enqueue_norm_then(h, max_norm, inv_scale, out_norm, out_nonfinite_flag,
                            static_cast<cudaStream_t>(stream),
                            reinterpret_cast<const void*>(gclip::k_adamw), args);
+}
+
+extern "C" int clip_adamw_step(clip_handle_t h, const clip_adamw_params_t* p, int64_t step,
+                               void* stream) {
+  if (h == nullptr || p == nullptr || h->d_states == nullptr) return GCLIP_ERR_INVALID_ARG;
+  gclip::AdamwArgs q;
+  if (!adamw_args(p, step, q)) return GCLIP_ERR_INVALID_ARG;
+  int64_t nc = h->n_chunks;
+  if (nc == 0) return GCLIP_OK;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return GCLIP_ERR_CUDA;
+  const clip_chunk_t* chunks = h->d_chunks;
+  const gclip::TensorState* st = h->d_states;
+  const clip_result_t* unit = h->d_unit;
+  void* args[] = {&chunks, &nc, &st, &unit, &q};
+  if (launch_pdl(reinterpret_cast<const void*>(gclip::k_adamw), static_cast<unsigned int>(nc),
+                 static_cast<cudaStream_t>(stream), args, true) != cudaSuccess) {
+    cudaGetLastError();
+    return GCLIP_ERR_CUDA;
+  }
+  return GCLIP_OK;
 }
 
 extern "C" int clip_grad_norm_per_tensor(clip_handle_t h, float max_norm, float inv_scale,

@@ -379,6 +379,25 @@ int clip_grad_norm_adamw(clip_handle_t h, float max_norm, float inv_scale,
                          float *out_norm, int32_t *out_nonfinite_flag,
                          void *stream);
 
+/* clip_adamw_step -- one AdamW step of optimizer step number `step`
+ * (1-based) on the attached state with the gradients as they are: the second
+ * launch of clip_grad_norm_adamw alone, with multiplier 1 and no norm pass.
+ * For an update that follows a clip already made by clip_grad_norm (the
+ * clipping page, "Order matters: Pre-Adam": clip, then AdamW), and the
+ * unfused counterpart the fused call is measured against.  For fp32
+ * gradients, clip_grad_norm followed by this call gives w, m and v bit for
+ * bit equal to clip_grad_norm_adamw (the in-place clip stores exactly the
+ * fp32 value the fused pass forms in registers); for fp16/bf16 gradients
+ * the clipped values are rounded to the gradient's format first.  Nonfinite
+ * gradients are not checked: they reach the moments as they are.  The
+ * gradients are read, and set to +0 if p->zero_grads.  Asynchronous, no
+ * allocation, nothing written to the record.  Returns GCLIP_OK (also for a
+ * set with no elements); GCLIP_ERR_INVALID_ARG (NULL handle or p, no state
+ * attached, a hyperparameter or step out of range as for
+ * clip_grad_norm_adamw); GCLIP_ERR_CUDA if the launch failed. */
+int clip_adamw_step(clip_handle_t h, const clip_adamw_params_t *p, int64_t step,
+                    void *stream);
+
 /* ---- per-tensor clipping -------------------------------------------------
  *
  * Source: the clipping page, section "Per-Tensor or Global": each gradient

@@ -61,21 +61,31 @@ def make_states(tensors, seed, fresh=False, misalign=False):
     return out, keep
 
 
-def check(tensors, states, max_norm, inv_scale, hp, step, zero_grads=False, name=""):
+def check(tensors, states, max_norm, inv_scale, hp, step, zero_grads=False, name="", alone=False):
+    """alone: clip_adamw_step (the AdamW step with the gradients as they
+    are), against the oracle's clip + AdamW at a threshold no norm reaches and
+    inv_scale 1 (multiplier 1)."""
     hp = {k: f32(v) for k, v in hp.items()}
     max_norm, inv_scale = f32(max_norm), f32(inv_scale)
     g_host = [to_oracle(t) for t in tensors]
     s_host = [tuple(a.detach().cpu().numpy().copy() for a in st) for st in states]
     with g.GradClipper(tensors) as c:
         c.attach_adamw(states)
-        norm, flag = c.clip_adamw_(max_norm, inv_scale, step=step, zero_grads=zero_grads, **hp)
-        rec = c.result()
+        if alone:
+            c.adamw_step_(step=step, zero_grads=zero_grads, **hp)
+            torch.cuda.synchronize()
+        else:
+            norm, flag = c.clip_adamw_(max_norm, inv_scale, step=step, zero_grads=zero_grads, **hp)
+            rec = c.result()
     grads_want, new, r = oracle.default().clip_adamw(g_host, s_host, max_norm, inv_scale,
                                                      step=step, zero_grads=zero_grads, **hp)
-    assert rec["decision"] == r.decision and bool(rec["nonfinite"]) == r.nonfinite, name
-    assert int(flag.item()) == int(r.nonfinite)
-    if not r.nonfinite:
-        assert abs(rec["norm"] - r.norm) <= 1e-5 * r.norm, (name, rec["norm"], r.norm)
+    if alone:
+        assert r.decision == oracle.PASS and r.coef == 1.0 and inv_scale == 1.0, (name, r.norm)
+    else:
+        assert rec["decision"] == r.decision and bool(rec["nonfinite"]) == r.nonfinite, name
+        assert int(flag.item()) == int(r.nonfinite)
+        if not r.nonfinite:
+            assert abs(rec["norm"] - r.norm) <= 1e-5 * r.norm, (name, rec["norm"], r.norm)
     bc1 = 1 - hp["beta1"] ** step
     bc2 = 1 - hp["beta2"] ** step
     worst = 0.0
@@ -120,6 +130,48 @@ def test_fused_matches_oracle(name, step, fresh):
     gs = make_gradset(name, device=dev())
     states, _ = make_states(gs.tensors, 7, fresh=fresh)
     check(gs.tensors, states, gs.max_norm, gs.inv_scale, HP, step, name=name)
+
+
+@pytest.mark.parametrize("name,step", [("tiny", 1), ("andrea14m", 4), ("andrea120m_bf16", 2)])
+def test_step_alone_matches_oracle(name, step):
+    """clip_adamw_step: AdamW with the gradients as they are."""
+    gs = make_gradset(name, device=dev())
+    states, _ = make_states(gs.tensors, 13)
+    check(gs.tensors, states, 3.0e38, 1.0, HP, step, name=name, alone=True)
+
+
+def test_step_alone_zero_grads_and_misaligned_state():
+    gs = make_gradset("andrea14m", device=dev())
+    states, keep = make_states(gs.tensors, 17, misalign=True)
+    check(gs.tensors, states, 3.0e38, 1.0, HP, 3, zero_grads=True, name="alone zero+misaligned",
+          alone=True)
+
+
+@pytest.mark.parametrize("name", ["andrea120m", "andrea14m"])
+def test_clip_then_step_equals_fused(name):
+    """For fp32 gradients, clip_grad_norm followed by clip_adamw_step leaves
+    w, m and v bit for bit where clip_grad_norm_adamw does: the in-place clip
+    stores exactly the fp32 value the fused pass forms in registers."""
+    gs = make_gradset(name, device=dev())
+    grads_a = [t.clone() for t in gs.tensors]
+    grads_b = [t.clone() for t in gs.tensors]
+    states_a, _ = make_states(gs.tensors, 19)
+    states_b = [tuple(a.clone() for a in st) for st in states_a]
+    with g.GradClipper(grads_a) as ca, g.GradClipper(grads_b) as cb:
+        ca.attach_adamw(states_a)
+        cb.attach_adamw(states_b)
+        for step in (1, 2):
+            ca.clip_adamw_(gs.max_norm, gs.inv_scale, step=step, **HP)
+            for t, o in zip(grads_b, gs.tensors):    # the fused call only reads its gradients
+                t.copy_(o)
+            cb.clip_(gs.max_norm, gs.inv_scale)
+            cb.adamw_step_(step=step, **HP)
+            torch.cuda.synchronize()
+            assert ca.result()["decision"] == cb.result()["decision"]
+            assert ca.result()["norm"] == cb.result()["norm"]
+        for sa, sb in zip(states_a, states_b):
+            for a, b in zip(sa, sb):
+                assert torch.equal(a, b)
 
 
 def test_zero_grads_and_misaligned_state():
@@ -172,4 +224,15 @@ def test_argument_checks():
                 c.clip_adamw_(1.0, **kw)
         with pytest.raises(g.GclipError):
             c.clip_adamw_(1.0, lr=1e-3, step=0)
+        for bad in (dict(lr=-1.0), dict(beta1=1.0), dict(eps=0.0), dict(step=0)):
+            kw = dict(lr=1e-3, step=1)
+            kw.update(bad)
+            with pytest.raises(g.GclipError):
+                c.adamw_step_(**kw)
+        assert L.clip_adamw_step(None, p, 1, None) == g._abi.GCLIP_ERR_INVALID_ARG
+        assert L.clip_adamw_step(c._h, None, 1, None) == g._abi.GCLIP_ERR_INVALID_ARG
+    with g.GradClipper([x]) as c:
+        L = g.load()
+        p = g._abi.clip_adamw_params_t(1e-3, 0.9, 0.999, 1e-8, 0.0, 0)
+        assert L.clip_adamw_step(c._h, p, 1, None) == g._abi.GCLIP_ERR_INVALID_ARG  # no state
     assert x.cpu().tolist() == [1.0] * 8
